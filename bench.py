@@ -1,0 +1,394 @@
+"""Benchmark of the attention forward pass on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one attention forward (the whole hot path) over one batch of seeded
+synthetic input. The default workload is the long-sequence causal one
+(B=2 H=16 N=8192 d=128, bf16), whose Q, K, V (201 MB) exceed the 129 MB L2,
+so no flush is needed between steps. FLOPs are counted as 4*B*H*N^2*d, halved
+under causal masking.
+
+Under torchrun each rank runs an independent replica on its own GPU (the work
+units share nothing), so the value is the total FLOPs of all ranks over the
+slowest rank's time ("weak" scaling).
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload (the pages ship no runnable code; the
+oracle is the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 (bf16) and fraction of dense BF16 peak"
+UNIT = "TFLOP/s"
+KERNEL_SOURCES = ("blocked_online_softmax_gb300/csrc",)
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="causal_b2h16n8192d128")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle sample time")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for d in KERNEL_SOURCES:
+        base = os.path.join(ROOT, d)
+        for name in sorted(os.listdir(base)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(base, name), "rb") as f:
+                    h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload_name}_traffic.txt")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    fields[key.strip()] = val.strip()
+        if fields.get("kernel_source_sha") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        self.t0 = time.time()
+
+    def mark(self):
+        self.t_start = time.time()
+
+    def stop(self):
+        self.t_end = time.time()
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        return self.summarise(rows)
+
+    @staticmethod
+    def summarise(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, val in zip(names, r[5:9]) if val.lower() == "active"})
+        # samples taken while the kernel ran (the GPU at least half-way up its clock range)
+        loaded = [s for s in sm if s >= 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if _isnum(r[3]))
+                if any(_isnum(r[3]) for r in rows) else None}
+
+
+def _isnum(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+def oracle_rows_flops(w, rows):
+    """FLOPs of the sampled rows by the same rule as the metric: 4*d per visited (row, key) pair."""
+    import numpy as np
+    i = np.asarray(rows) % w.N
+    keys = (i + 1) if w.causal else np.full_like(i, w.N)
+    return float(4.0 * w.d * keys.sum())
+
+
+def time_oracle(w, q, k, v, target_seconds):
+    """Time the oracle as it stands on evenly spaced rows of head 0, about target_seconds long."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    probe = np.arange(0, w.N, max(1, w.N // 64), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, rows=probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    per_flop = dt / oracle_rows_flops(w, probe)
+    # grow the sample to about target_seconds; whole heads first, then strided rows of one head
+    head_flops = oracle_rows_flops(w, np.arange(w.N))
+    n_heads = int(max(0, min(w.B * w.H, target_seconds / (per_flop * head_flops))))
+    if n_heads >= 1:
+        rows = np.arange(n_heads * w.N, dtype=np.int64)
+        desc = f"{n_heads} whole head(s) of {w.B * w.H} ({n_heads * w.N} query rows)"
+    else:
+        stride = max(1, int(math.ceil(head_flops * per_flop / max(target_seconds, 1e-3))))
+        rows = np.arange(0, w.N, stride, dtype=np.int64)
+        desc = f"every {stride}th query row of head 0 ({rows.size} rows)"
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = oracle_rows_flops(w, rows)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{desc}; fp64 C oracle, three-pass softmax over materialised score rows; "
+                      f"{dt:.2f} s", "seconds": dt, "host_cpus": len(os.sched_getaffinity(0))}
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 oracle on the host cores, bounded per-step samples."""
+    import numpy as np
+
+    import oracle
+    from blocked_online_softmax_gb300.workloads import workload_qkv
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    oracle.build()
+    cores = oracle.max_threads()
+    q, k, v = workload_qkv(w)
+    budget = 120.0 / max(1, args.steps + args.warmup)         # seconds per step
+    probe = np.arange(0, w.N, max(1, w.N // 32), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, rows=probe)
+    per_flop = (time.perf_counter() - t0) / oracle_rows_flops(w, probe)
+    head_flops = oracle_rows_flops(w, np.arange(w.N))
+    stride = max(1, int(math.ceil(head_flops * per_flop / budget)))
+    rows = np.arange(0, w.N, stride, dtype=np.int64)
+    flops = oracle_rows_flops(w, rows)
+    for _ in range(args.warmup):
+        oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    value = flops * args.steps / dt / 1e12
+    sample = (f"per step: every {stride}th query row of head 0 ({rows.size} rows) of {w.name}; "
+              f"fp64 C oracle on {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    in_bytes = 3 * w.B * w.H * w.N * w.d * 2
+    return {"workload": w.describe(), "name": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "causal": w.causal, "scale": w.scale, "logit_mult": w.logit_mult,
+            "flops_per_step": w.flops, "parallelism": "replicas (one per GPU)",
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > 129 MB), no flush"
+            if in_bytes > 129e6 else "L2 flushed between steps"}
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import blocked_online_softmax_gb300 as bos
+    from blocked_online_softmax_gb300 import _build
+    from blocked_online_softmax_gb300.workloads import workload_qkv
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    bos.load_library()
+
+    q_h, k_h, v_h = workload_qkv(w)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    in_bytes = 3 * q.numel() * 2
+    flush = None
+    if in_bytes <= 129e6:
+        flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        if flush is not None:
+            flush.zero_()
+        bos.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark()
+    with torch.cuda.stream(stream):
+        t_begin.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            bos.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+            ends[i].record(stream)
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = w.flops * args.steps * world / (total_ms / 1e3) / 1e12
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    op = torch.empty_like(q_h).pin_memory()
+    lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 200))
+    bos.attn_fwd_host(qp, kp, vp, op, lp, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        bos.attn_fwd_host(qp, kp, vp, op, lp, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = w.flops * e2e_steps * world / e2e_s / 1e12
+
+    peaks, peaks_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    avg_launch_ms = statistics.fmean(launch_ms)
+    achieved = w.flops / (avg_launch_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                "peak_kind": f"{peaks_kind} dense bf16 burst (cuBLAS)",
+                "kernel": "attn_fwd", "median_launch_ms": statistics.median(launch_ms),
+                "algorithmic_bytes": 8.0 * w.B * w.H * w.N * w.d + 4.0 * w.B * w.H * w.N,
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, q_h, k_h, v_h, args.cpu_seconds)
+
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w),
+            "frac_of_peak": value / world / peak,
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
+                    "h2d_bytes_per_step": int(in_bytes),
+                    "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
+                    "api": "attn_fwd_host (pinned host buffers; copies, kernel, copies back, sync)"},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "kernel_source_sha": kernel_source_hash()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    from blocked_online_softmax_gb300.workloads import BY_NAME
+    if args.workload not in BY_NAME:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(BY_NAME)}")
+    w = BY_NAME[args.workload]
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,137 @@
+"""Python binding of the GB300 attention-forward library (ctypes over the C ABI).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``libbos_attn.so`` built from ``csrc/`` (see ``include/attn.h`` for the
+contract). There is no CPU or PyTorch fallback: if the library is missing or
+the GPU is not sm_103a, the calls raise.
+
+Names follow the C ABI: ``attn_fwd``, ``attn_fwd_host``, ``attn_status_string``.
+``attention`` is a convenience that allocates O and LSE with torch (device
+memory only) and calls ``attn_fwd``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbos_attn.so")
+
+# status codes, mirrored from include/attn.h
+ATTN_OK = 0
+ATTN_ERR_NULLPTR = 1
+ATTN_ERR_BAD_SHAPE = 2
+ATTN_ERR_UNSUPPORTED_D = 3
+ATTN_ERR_BAD_SCALE = 4
+ATTN_ERR_MISALIGNED = 5
+ATTN_ERR_UNSUPPORTED_DEVICE = 6
+ATTN_ERR_LAUNCH = 7
+ATTN_ERR_TIMEOUT = 8
+ATTN_ERR_CUDA = 9
+ATTN_ERR_BAD_ARG = 10
+
+# every symbol include/attn.h declares
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_status_string", "attn_abi_version")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: status {status}: {attn_status_string(status)}")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built ({path} missing): run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    for name in ("attn_fwd", "attn_fwd_host"):
+        fn = getattr(lib, name)
+        fn.restype = i
+        fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_abi_version.restype = i
+    lib.attn_abi_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_abi_version() -> int:
+    return int(load_library().attn_abi_version())
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):           # numpy array
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot take a pointer from {type(x)!r}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal,
+             stream=None) -> None:
+    """Enqueue the forward kernel (C ``attn_fwd``); raises AttnError on a nonzero status.
+
+    q, k, v, o: bf16 device tensors (or raw device pointers), contiguous [B,H,N,d];
+    lse: fp32 device tensor [B,H,N]; stream: torch stream, raw handle, or None
+    for torch's current stream.
+    """
+    st = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                 int(N), int(d), float(scale), int(causal), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+
+
+def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B: int, H: int, N: int, d: int, scale: float,
+                  causal, stream=None) -> None:
+    """Host-buffer entry (C ``attn_fwd_host``): copies in, runs, copies out, synchronises."""
+    st = load_library().attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h),
+                                      int(B), int(H), int(N), int(d), float(scale), int(causal),
+                                      _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_host")
+
+
+def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None):
+    """O, LSE for bf16 CUDA tensors [B,H,N,d]; scale defaults to 1/sqrt(d) rounded to fp32."""
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must be [B,H,N,d] with one shape")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+    return o, lse

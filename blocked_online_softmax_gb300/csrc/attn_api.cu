@@ -1,0 +1,143 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// device check, dispatch to the sm_103a kernel, and the host-buffer path.
+//
+// The operation is the forward pass of "4.4 Writing GPU Kernels with Triton"
+// (llm-stack-book), Kernel 4 "A Simplified FlashAttention"; the page's wrapper
+// `flash_attention` allocates O like q and an fp32 (B, H, N) LSE and launches
+// one program per (query block, batch*head). Here the caller owns all buffers
+// and every argument is checked before anything is launched.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int kMaxDevices = 64;
+
+// Per-device cache of the compute-capability check: 0 unknown, 1 ok, 2 unsupported.
+int g_device_ok[kMaxDevices] = {0};
+std::mutex g_device_mu;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks that need no GPU. Returns ATTN_OK or the first failing status.
+int validate_host(const void* q, const void* k, const void* v, const void* o, const void* lse,
+                  int B, int H, int N, int d, float scale, int causal, bool device_ptrs) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULLPTR;
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_BAD_SHAPE;
+    const int64_t rows = (int64_t)B * H * N;
+    if ((int64_t)B * H > INT_MAX || rows > ((int64_t)1 << 40)) return ATTN_ERR_BAD_SHAPE;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_D;
+    if (!std::isfinite(scale)) return ATTN_ERR_BAD_SCALE;
+    if (causal != 0 && causal != 1) return ATTN_ERR_BAD_ARG;
+    if (device_ptrs) {
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+            return ATTN_ERR_MISALIGNED;
+        if (!aligned(lse, 4)) return ATTN_ERR_MISALIGNED;
+    }
+    return ATTN_OK;
+}
+
+int check_device(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return ATTN_ERR_CUDA; }
+    *dev_out = dev;
+    if (dev >= 0 && dev < kMaxDevices && g_device_ok[dev] != 0)
+        return g_device_ok[dev] == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lk(g_device_mu);
+        g_device_ok[dev] = ok ? 1 : 2;
+    }
+    return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int N, int d, float scale, int causal, void* stream) {
+    int st = validate_host(q, k, v, o, lse, B, H, N, d, scale, causal, true);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+    bos::AttnParams p;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.B = B; p.H = H; p.N = N; p.d = d;
+    p.scale = scale; p.causal = causal;
+    return bos::launch_attn_fwd(p, static_cast<cudaStream_t>(stream), dev);
+}
+
+extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                             float* lse_h, int B, int H, int N, int d, float scale, int causal,
+                             void* stream_) {
+    int st = validate_host(q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal, false);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const size_t elems = (size_t)B * H * N * d;
+    const size_t tbytes = elems * 2;                      // bf16
+    const size_t lbytes = (size_t)B * H * N * sizeof(float);
+    // One staging block: Q | K | V | O | LSE, each sub-buffer 256-byte aligned.
+    auto round_up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t off_k = round_up(tbytes), off_v = off_k + round_up(tbytes),
+                 off_o = off_v + round_up(tbytes), off_l = off_o + round_up(tbytes),
+                 total = off_l + round_up(lbytes);
+    char* base = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&base), total, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    int rc = ATTN_OK;
+    if (cudaMemcpyAsync(base, q_h, tbytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(base + off_k, k_h, tbytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(base + off_v, v_h, tbytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+        rc = ATTN_ERR_CUDA;
+    }
+    if (rc == ATTN_OK)
+        rc = attn_fwd(base, base + off_k, base + off_v, base + off_o,
+                      reinterpret_cast<float*>(base + off_l), B, H, N, d, scale, causal, stream);
+    if (rc == ATTN_OK &&
+        (cudaMemcpyAsync(o_h, base + off_o, tbytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+         cudaMemcpyAsync(lse_h, base + off_l, lbytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)) {
+        rc = ATTN_ERR_CUDA;
+    }
+    cudaFreeAsync(base, stream);
+    if (cudaStreamSynchronize(stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    if (rc != ATTN_OK) cudaGetLastError();
+    return rc;
+}
+
+extern "C" const char* attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_NULLPTR: return "a required pointer is NULL";
+        case ATTN_ERR_BAD_SHAPE: return "B, H and N must be >= 1 and the sizes must fit the index space";
+        case ATTN_ERR_UNSUPPORTED_D: return "head dimension d must be 64 or 128";
+        case ATTN_ERR_BAD_SCALE: return "scale must be finite";
+        case ATTN_ERR_MISALIGNED: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";
+        case ATTN_ERR_UNSUPPORTED_DEVICE: return "the current device is not compute capability 10.3 (sm_103a)";
+        case ATTN_ERR_LAUNCH: return "kernel launch failed";
+        case ATTN_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
+        case ATTN_ERR_CUDA: return "a CUDA runtime call failed";
+        case ATTN_ERR_BAD_ARG: return "malformed argument (causal must be 0 or 1)";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int attn_abi_version(void) { return kAbiVersion; }

@@ -1,0 +1,23 @@
+// Internal interface between the C-ABI host code and the device kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace bos {
+
+struct AttnParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int B, H, N, d;
+    float scale;
+    int causal;
+};
+
+// Enqueues the forward kernel for validated arguments on `stream` (device `dev`
+// is current). Returns an attn_status code.
+int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev);
+
+}  // namespace bos

@@ -1,0 +1,100 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) attention-forward library.
+ *
+ * The operation is the forward pass of "4.4 Writing GPU Kernels with Triton"
+ * (llm-stack-book), Kernel 4 "A Simplified FlashAttention", with the online
+ * softmax of "The Online Softmax Recurrence" on the same page: per (batch,
+ * head),
+ *
+ *     O[i, :] = sum_j softmax_j(scale * q_i . k_j) v_j
+ *     LSE[i]  = ln sum_j exp(scale * q_i . k_j)            (natural log)
+ *
+ * with key j > i masked when causal is set (top-left aligned, as torch.tril).
+ * The N x N score matrix is never written to memory: key/value tiles are
+ * streamed through on-chip memory and each query row keeps a running max, a
+ * running sum and an unnormalised accumulator, normalised once at the end.
+ * LSE is saved in natural log (the kernel runs in base 2 internally), as the
+ * page's "Base consistency" note asks, so a backward pass can rebuild P with a
+ * plain exp.
+ *
+ * Nothing here allocates on behalf of the caller except attn_fwd_host, which
+ * stages host buffers through stream-ordered device memory.
+ */
+#ifndef BOS_ATTN_H
+#define BOS_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. Every entry point returns one; 0 means success. */
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_NULLPTR = 1,            /* a required pointer is NULL */
+    ATTN_ERR_BAD_SHAPE = 2,          /* B, H or N < 1, or the sizes overflow the index space */
+    ATTN_ERR_UNSUPPORTED_D = 3,      /* d is not one of the compiled head dims (64, 128) */
+    ATTN_ERR_BAD_SCALE = 4,          /* scale is NaN or infinite */
+    ATTN_ERR_MISALIGNED = 5,         /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
+    ATTN_ERR_UNSUPPORTED_DEVICE = 6, /* the current device is not compute capability 10.3 */
+    ATTN_ERR_LAUNCH = 7,             /* the kernel launch failed (cudaGetLastError) */
+    ATTN_ERR_TIMEOUT = 8,            /* a bounded wait inside the kernel gave up */
+    ATTN_ERR_CUDA = 9,               /* another CUDA runtime call failed */
+    ATTN_ERR_BAD_ARG = 10            /* causal not 0/1, or another malformed argument */
+} attn_status;
+
+/*
+ * attn_fwd - attention forward on device buffers, asynchronous on `stream`.
+ *
+ *   q, k, v : bf16, contiguous [B, H, N, d] (row i of head (b, h) at element
+ *             ((b*H + h)*N + i)*d), device memory, 16-byte aligned. Read only.
+ *   o       : bf16, contiguous [B, H, N, d], device memory, 16-byte aligned.
+ *             Written, rounded to nearest even from the fp32 accumulator.
+ *   lse     : fp32, contiguous [B, H, N], device memory, 4-byte aligned.
+ *             Written with the natural-log log-sum-exp of each row.
+ *   B, H, N : batch, heads, sequence length; each >= 1. N need not be a
+ *             multiple of any tile size: keys past N do not exist and rows past
+ *             N are neither read as outputs nor written.
+ *   d       : head dimension, 64 or 128.
+ *   scale   : the multiplier of q . k (1/sqrt(d) in the pages; a C ABI has no
+ *             default, so the caller passes it). Must be finite.
+ *   causal  : 0 or 1. With 1, query i attends to keys 0..i.
+ *   stream  : a cudaStream_t (NULL = the legacy default stream).
+ *
+ * The caller owns every buffer. The call validates all arguments on the host
+ * first; on any error it returns a nonzero status and launches nothing and
+ * writes nothing. On success the kernel is enqueued on `stream` and the call
+ * returns without synchronising. Safe to call from several host threads.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * attn_fwd_host - the same operation on HOST buffers, end to end.
+ *
+ *   q_h, k_h, v_h : bf16 host arrays, contiguous [B, H, N, d] (pinned memory
+ *                   gives full copy bandwidth; pageable memory also works).
+ *   o_h           : bf16 host array [B, H, N, d], written.
+ *   lse_h         : fp32 host array [B, H, N], written.
+ *   other arguments as for attn_fwd.
+ *
+ * Copies the inputs to stream-ordered device memory (cudaMallocAsync on
+ * `stream`), runs attn_fwd, copies O and LSE back, frees the staging memory
+ * and synchronises `stream` before returning, so the host arrays are ready
+ * when it returns ATTN_OK. Host pointers need no particular alignment.
+ */
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                  int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/* Human-readable text for a status code; never NULL, static storage. */
+const char* attn_status_string(int status);
+
+/* Version of this ABI (incremented on any incompatible change). */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BOS_ATTN_H */

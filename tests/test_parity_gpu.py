@@ -1,0 +1,141 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small and medium sizes are compared element by element over every output;
+the full-size workloads are compared on sampled rows (tile edges, the ragged
+tail, random rows) plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import blocked_online_softmax_gb300 as bos
+import oracle
+from blocked_online_softmax_gb300.workloads import (CAUSAL_2K, CAUSAL_8K, MEDIUM, SMALL, TAIL_4000,
+                                                    make_qkv, workload_qkv)
+from parity_util import assert_parity, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+SENT_BF16 = -12288.0      # exactly representable in bf16 (-3 * 2^12)
+SENT_F32 = -7.0e30
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def run_guarded(q, k, v, scale, causal, stream=None):
+    """attn_fwd into canary-guarded O / LSE; checks the guards; returns host O (float) and LSE."""
+    B, H, N, d = q.shape
+    pad_o, pad_l = 64, 16                       # keep 16-byte alignment of the views
+    n_o, n_l = B * H * N * d, B * H * N
+    dev = torch.device("cuda")
+    o_buf = torch.full((pad_o + n_o + pad_o,), SENT_BF16, dtype=torch.bfloat16, device=dev)
+    l_buf = torch.full((pad_l + n_l + pad_l,), SENT_F32, dtype=torch.float32, device=dev)
+    o = o_buf[pad_o:pad_o + n_o].view(B, H, N, d)
+    lse = l_buf[pad_l:pad_l + n_l].view(B, H, N)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    bos.attn_fwd(qd, kd, vd, o, lse, B, H, N, d, scale, causal, stream)
+    torch.cuda.synchronize()
+    ob, lb = o_buf.float().cpu(), l_buf.cpu()
+    assert torch.all(ob[:pad_o] == SENT_BF16) and torch.all(ob[pad_o + n_o:] == SENT_BF16), "O guard overwritten"
+    assert torch.all(lb[:pad_l] == SENT_F32) and torch.all(lb[pad_l + n_l:] == SENT_F32), "LSE guard overwritten"
+    return ob[pad_o:pad_o + n_o].view(B, H, N, d).numpy(), lb[pad_l:pad_l + n_l].view(B, H, N).numpy()
+
+
+# ------------------------------------------------------------------ full comparison
+
+@pytest.mark.parametrize("w", [SMALL, MEDIUM], ids=lambda w: w.name)
+def test_workload_full(w):
+    q, k, v = workload_qkv(w)
+    o, lse = run_guarded(q, k, v, w.scale, w.causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
+    assert_parity(o, lse, o_ref, lse_ref, w.name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 2, 31, 127, 128, 129, 255, 256, 257, 383, 600])
+def test_edge_lengths(N, d, causal):
+    q, k, v = make_qkv(1, 2, N, d, seed=1000 + N + d)
+    scale = float(np.float32(d ** -0.5))
+    o, lse = run_guarded(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    assert_parity(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_several_tiles_ragged_tail(d, causal):
+    """Several query/key tiles, odd batch and head counts, a ragged tail."""
+    B, H, N = 2, 3, 1000
+    q, k, v = make_qkv(B, H, N, d, seed=77 + d)
+    scale = float(np.float32(d ** -0.5))
+    o, lse = run_guarded(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    assert_parity(o, lse, o_ref, lse_ref, f"B2H3N1000 d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("mult", [4.0, 8.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_logits_stability(mult, causal):
+    q, k, v = make_qkv(1, 2, 700, 64, seed=5, logit_mult=mult)
+    o, lse = run_guarded(q, k, v, 0.125, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, 0.125, causal)
+    assert_parity(o, lse, o_ref, lse_ref, f"x{mult} causal={causal}")
+
+
+def test_scale_zero_and_negative():
+    q, k, v = make_qkv(1, 1, 300, 128, seed=9)
+    for scale in (0.0, -0.2):
+        o, lse = run_guarded(q, k, v, scale, False)
+        o_ref, lse_ref = oracle.attention(q, k, v, scale, False)
+        assert_parity(o, lse, o_ref, lse_ref, f"scale={scale}")
+
+
+def test_side_stream_and_determinism():
+    q, k, v = make_qkv(2, 2, 513, 128, seed=11)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = run_guarded(q, k, v, 0.0883883, True, stream=s)
+    o2, l2 = run_guarded(q, k, v, 0.0883883, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    o_ref, lse_ref = oracle.attention(q, k, v, float(np.float32(0.0883883)), True)
+    assert_parity(o1, l1, o_ref, lse_ref, "side stream")
+
+
+def test_host_buffer_entry():
+    B, H, N, d = 1, 3, 333, 64
+    q, k, v = make_qkv(B, H, N, d, seed=12)
+    o = torch.empty_like(q).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    bos.attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), o, lse, B, H, N, d, 0.125, 1)
+    o_ref, lse_ref = oracle.attention(q, k, v, 0.125, True)
+    assert_parity(o.float().numpy(), lse.numpy(), o_ref, lse_ref, "host entry")
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+
+@pytest.mark.parametrize("w", [MEDIUM, CAUSAL_2K, CAUSAL_8K, TAIL_4000], ids=lambda w: w.name)
+def test_workload_full_size_sampled(w):
+    q, k, v = workload_qkv(w)
+    o, lse = run_guarded(q, k, v, w.scale, w.causal)
+    # properties at every row: finite, and O a convex combination of V rows per column
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    vf = v.float()
+    if not w.causal:
+        vmax = vf.amax(dim=2, keepdim=True).numpy()
+        vmin = vf.amin(dim=2, keepdim=True).numpy()
+    else:
+        vmax = torch.cummax(vf, dim=2).values.numpy()
+        vmin = torch.cummin(vf, dim=2).values.numpy()
+    slack = 1e-2 + 2 ** -7 * np.maximum(np.abs(vmax), np.abs(vmin))
+    assert np.all(o <= vmax + slack) and np.all(o >= vmin - slack), "O outside the hull of V"
+    rows = sample_rows(w.B, w.H, w.N, seed=w.seed)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
+    d = w.d
+    assert_parity(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.name)
