@@ -34,7 +34,8 @@ ATTN_ERR_CUDA = 9
 ATTN_ERR_BAD_ARG = 10
 
 # every symbol include/attn.h declares
-EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_status_string", "attn_abi_version")
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_device_status", "attn_set_wait_limit_ns",
+                    "attn_status_string", "attn_abi_version")
 
 _lib = None
 
@@ -59,6 +60,10 @@ def load_library(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = i
         fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.attn_device_status.restype = i
+    lib.attn_device_status.argtypes = [vp]
+    lib.attn_set_wait_limit_ns.restype = i
+    lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i]
     lib.attn_abi_version.restype = i
@@ -118,6 +123,16 @@ def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B: int, H: int, N: int, d: int, sca
                                       _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_host")
+
+
+def attn_device_status(stream=None) -> int:
+    """Synchronise the stream, return and clear the kernel's sticky status word (C ``attn_device_status``)."""
+    return int(load_library().attn_device_status(_stream_handle(stream)))
+
+
+def attn_set_wait_limit_ns(ns: int) -> None:
+    """Wall-time limit of each wait inside the kernel (0 = default 2 s)."""
+    load_library().attn_set_wait_limit_ns(int(ns))
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None):

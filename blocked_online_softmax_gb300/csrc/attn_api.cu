@@ -33,7 +33,9 @@ int validate_host(const void* q, const void* k, const void* v, const void* o, co
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULLPTR;
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_BAD_SHAPE;
     const int64_t rows = (int64_t)B * H * N;
-    if ((int64_t)B * H > INT_MAX || rows > ((int64_t)1 << 40)) return ATTN_ERR_BAD_SHAPE;
+    const int64_t units = (int64_t)B * H * ((N + 255) / 256);   // 256-row work units
+    if ((int64_t)B * H > INT_MAX || rows > ((int64_t)1 << 40) || units > INT_MAX / 2)
+        return ATTN_ERR_BAD_SHAPE;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return ATTN_ERR_BAD_SCALE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_ARG;
@@ -121,6 +123,18 @@ extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, 
     if (cudaStreamSynchronize(stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
     if (rc != ATTN_OK) cudaGetLastError();
     return rc;
+}
+
+extern "C" int attn_device_status(void* stream) {
+    int dev = 0;
+    const int st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+    return bos::read_and_clear_device_status(static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_set_wait_limit_ns(unsigned long long ns) {
+    bos::set_wait_limit_ns((uint64_t)ns);
+    return ATTN_OK;
 }
 
 extern "C" const char* attn_status_string(int status) {

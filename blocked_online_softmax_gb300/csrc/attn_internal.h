@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 namespace bos {
 
 struct AttnParams {
@@ -19,5 +21,12 @@ struct AttnParams {
 // Enqueues the forward kernel for validated arguments on `stream` (device `dev`
 // is current). Returns an attn_status code.
 int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev);
+
+// Wall-time limit of every wait inside the kernel (0 restores the default).
+void set_wait_limit_ns(uint64_t ns);
+
+// Synchronises `stream`, returns the sticky device status (an attn_status) and
+// clears it.
+int read_and_clear_device_status(cudaStream_t stream);
 
 }  // namespace bos

@@ -87,6 +87,25 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/*
+ * attn_device_status - failures that only the kernel can see.
+ *
+ * Every wait inside the kernel is bounded in wall time. A wait that runs out
+ * records ATTN_ERR_TIMEOUT in a device-wide status word and the kernel returns
+ * early (its outputs are then incomplete) after draining its own copies and
+ * MMAs, so the CUDA context stays usable. This call synchronises `stream`,
+ * returns that word (ATTN_OK if nothing failed since the last call) and clears
+ * it. The word is shared by all launches on the current device.
+ */
+int attn_device_status(void* stream);
+
+/*
+ * attn_set_wait_limit_ns - wall-time limit of each wait inside the kernel, in
+ * nanoseconds, for launches enqueued after the call (0 restores the default,
+ * 2 s). Process-wide. Intended for tests of the failure path.
+ */
+int attn_set_wait_limit_ns(unsigned long long ns);
+
 /* Human-readable text for a status code; never NULL, static storage. */
 const char* attn_status_string(int status);
 

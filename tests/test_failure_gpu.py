@@ -1,0 +1,61 @@
+"""Failure detection without a GPU fault: every wait inside the kernel is bounded.
+
+A wait limit of 1 ns makes the kernel's waits run out on purpose. The kernel
+must record ATTN_ERR_TIMEOUT, drain its own copies and MMAs, free tensor
+memory and return; the host reads the status and the context stays usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import blocked_online_softmax_gb300 as bos
+import oracle
+from blocked_online_softmax_gb300.workloads import make_qkv
+from parity_util import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _run(q, k, v, scale, causal):
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    bos.attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal)
+    return o, lse
+
+
+def test_status_ok_after_normal_runs():
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 300, 128, seed=21))
+    assert bos.attn_device_status() == bos.ATTN_OK
+    _run(q, k, v, 0.088, True)
+    assert bos.attn_device_status() == bos.ATTN_OK
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_wait_timeout_is_reported_and_context_survives(d, causal):
+    qh, kh, vh = make_qkv(2, 8, 1024, d, seed=22)
+    q, k, v = (t.cuda() for t in (qh, kh, vh))
+    assert bos.attn_device_status() == bos.ATTN_OK
+    statuses = []
+    bos.attn_set_wait_limit_ns(1)
+    try:
+        for _ in range(3):
+            _run(q, k, v, 0.1, causal)
+            statuses.append(bos.attn_device_status())
+    finally:
+        bos.attn_set_wait_limit_ns(0)
+    assert bos.ATTN_ERR_TIMEOUT in statuses
+    assert all(s in (bos.ATTN_OK, bos.ATTN_ERR_TIMEOUT) for s in statuses)
+    # the context is still usable and the next launch is correct
+    o, lse = _run(q, k, v, 0.1, causal)
+    assert bos.attn_device_status() == bos.ATTN_OK
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(qh, kh, vh, float(np.float32(0.1)), causal)
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "after timeout")
