@@ -48,6 +48,7 @@ def parse_args():
     ap.add_argument("--workload", default="causal_b2h16n8192d128")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle sample time")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     return ap.parse_args()
 
 
@@ -324,22 +325,24 @@ def run_ours(args, w):
     value = w.flops * args.steps * world / (total_ms / 1e3) / 1e12
 
     # end to end through the host-buffer entry point (pinned host memory)
-    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-    op = torch.empty_like(q_h).pin_memory()
-    lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-    e2e_steps = max(1, min(args.steps, 200))
-    bos.attn_fwd_host(qp, kp, vp, op, lp, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
-    if dist is not None:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    e2e_value, e2e_steps = None, 0
+    if not args.no_e2e:
+        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+        op = torch.empty_like(q_h).pin_memory()
+        lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        e2e_steps = max(1, min(args.steps, 200))
         bos.attn_fwd_host(qp, kp, vp, op, lp, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = w.flops * e2e_steps * world / e2e_s / 1e12
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            bos.attn_fwd_host(qp, kp, vp, op, lp, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+        e2e_s = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e_value = w.flops * e2e_steps * world / e2e_s / 1e12
 
     peaks, peaks_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))

@@ -35,7 +35,7 @@ ATTN_ERR_BAD_ARG = 10
 
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_device_status", "attn_set_wait_limit_ns",
-                    "attn_status_string", "attn_abi_version")
+                    "attn_set_test_stall", "attn_status_string", "attn_abi_version")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_device_status.argtypes = [vp]
     lib.attn_set_wait_limit_ns.restype = i
     lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.attn_set_test_stall.restype = i
+    lib.attn_set_test_stall.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i]
     lib.attn_abi_version.restype = i
@@ -133,6 +135,11 @@ def attn_device_status(stream=None) -> int:
 def attn_set_wait_limit_ns(ns: int) -> None:
     """Wall-time limit of each wait inside the kernel (0 = default 2 s)."""
     load_library().attn_set_wait_limit_ns(int(ns))
+
+
+def attn_set_test_stall(on: bool) -> None:
+    """Test hook: make every launch's MMA thread wait on a barrier nothing signals."""
+    load_library().attn_set_test_stall(int(bool(on)))
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None):

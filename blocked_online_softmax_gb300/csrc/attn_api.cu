@@ -137,6 +137,11 @@ extern "C" int attn_set_wait_limit_ns(unsigned long long ns) {
     return ATTN_OK;
 }
 
+extern "C" int attn_set_test_stall(int on) {
+    bos::set_test_stall(on);
+    return ATTN_OK;
+}
+
 extern "C" const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";

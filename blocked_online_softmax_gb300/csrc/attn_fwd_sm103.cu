@@ -68,8 +68,8 @@ struct Cfg {
     static constexpr int kBoxes = D / 64;                   // 64-column TMA boxes per tile
     static constexpr int kOffKV = 2 * kTileBytes;           // after the two Q tiles
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-    // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
-    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+    // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain, never
+    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 };
@@ -80,6 +80,7 @@ struct KernelArgs {
     __nv_bfloat16* o;
     float* lse;
     uint64_t wait_limit_ns;
+    int test_stall;   // test hook: the MMA thread first waits on a barrier nothing signals
 };
 
 }  // namespace
@@ -243,6 +244,7 @@ __device__ void mma_issuer(uint32_t tmem, const uint8_t* sQ, const uint8_t* sKV,
     uint64_t* p_full = s_full + 2;
     uint64_t* o_full = p_full + 2;
     uint64_t* drain = o_full + 2;
+    uint64_t* never = o_full + 3;
     const uint64_t lim = a.wait_limit_ns;
     const int total = a.BH * a.U;
     int stage = 0;
@@ -255,6 +257,7 @@ __device__ void mma_issuer(uint32_t tmem, const uint8_t* sQ, const uint8_t* sKV,
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         return got;
     };
+    if (a.test_stall && !wait_or_abort(never, 0, lim, abort_flag)) ok = false;
     int it = 0;
     for (int r = 0; ok; ++r, ++it) {
         const int k = unit_index(r);
@@ -473,6 +476,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             mbar_init(s_full + 4 + t, 1);                        // o_full
         }
         mbar_init(s_full + 6, 1);                                // drain
+        mbar_init(s_full + 7, 1);                                // never (test hook)
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -541,6 +545,7 @@ bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH,
 }
 
 uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
+int g_test_stall = 0;
 
 template <int D>
 int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
@@ -579,6 +584,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.o = static_cast<__nv_bfloat16*>(p.o);
     a.lse = p.lse;
     a.wait_limit_ns = g_wait_limit_ns;
+    a.test_stall = g_test_stall;
     const int64_t units = (int64_t)BH * a.U;
     const int grid = (int)(units < sms ? units : sms);
     attn_fwd_sm103_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
@@ -592,6 +598,8 @@ int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev) {
 }
 
 void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs; }
+
+void set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 
 int read_and_clear_device_status(cudaStream_t stream) {
     int h = 0;

@@ -25,6 +25,10 @@ int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev);
 // Wall-time limit of every wait inside the kernel (0 restores the default).
 void set_wait_limit_ns(uint64_t ns);
 
+// Test hook: launches enqueued while on make the MMA thread wait on a barrier
+// that nothing signals, so the bounded wait expires and the abort path runs.
+void set_test_stall(int on);
+
 // Synchronises `stream`, returns the sticky device status (an attn_status) and
 // clears it.
 int read_and_clear_device_status(cudaStream_t stream);

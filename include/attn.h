@@ -106,6 +106,15 @@ int attn_device_status(void* stream);
  */
 int attn_set_wait_limit_ns(unsigned long long ns);
 
+/*
+ * attn_set_test_stall - test hook for the failure path. While `on` is nonzero,
+ * every launch's MMA-issuing thread first waits on a barrier that nothing
+ * signals; the wait runs out after the wait limit, the kernel drains and
+ * returns, and attn_device_status reports ATTN_ERR_TIMEOUT. No fault, trap or
+ * hang is involved. Process-wide; off by default.
+ */
+int attn_set_test_stall(int on);
+
 /* Human-readable text for a status code; never NULL, static storage. */
 const char* attn_status_string(int status);
 
