@@ -32,10 +32,11 @@ ATTN_ERR_LAUNCH = 7
 ATTN_ERR_TIMEOUT = 8
 ATTN_ERR_CUDA = 9
 ATTN_ERR_BAD_ARG = 10
+ATTN_ERR_TOO_LARGE = 11
 
 # every symbol include/attn.h declares
-EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_device_status", "attn_set_wait_limit_ns",
-                    "attn_set_test_stall", "attn_status_string", "attn_abi_version")
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
+                    "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version")
 
 _lib = None
 
@@ -56,7 +57,7 @@ def load_library(path: str = LIB_PATH):
                            "`python -c 'import __graft_entry__ as g; g.build()'` first")
     lib = ctypes.CDLL(path)
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    for name in ("attn_fwd", "attn_fwd_host"):
+    for name in ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc"):
         fn = getattr(lib, name)
         fn.restype = i
         fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -125,6 +126,21 @@ def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B: int, H: int, N: int, d: int, sca
                                       _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_host")
+
+
+def attn_fwd_host_noalloc(q_h, k_h, v_h, o_h, lse_h, B: int, H: int, N: int, d: int, scale: float,
+                          causal, stream=None) -> None:
+    """Host-buffer entry that allocates no device memory (C ``attn_fwd_host_noalloc``).
+
+    For callers that cannot allocate device memory at the call site: staging goes
+    through one fixed device array shared by all calls, so calls must not overlap
+    on the GPU. Raises AttnError (ATTN_ERR_TOO_LARGE past the array's size).
+    """
+    st = load_library().attn_fwd_host_noalloc(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h),
+                                              int(B), int(H), int(N), int(d), float(scale), int(causal),
+                                              _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_host_noalloc")
 
 
 def attn_device_status(stream=None) -> int:

@@ -155,6 +155,7 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
         case ATTN_ERR_CUDA: return "a CUDA runtime call failed";
         case ATTN_ERR_BAD_ARG: return "malformed argument (causal must be 0 or 1)";
+        case ATTN_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of attn_fwd_host_noalloc (ATTN_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown status";
     }
 }

@@ -41,7 +41,8 @@ typedef enum attn_status {
     ATTN_ERR_LAUNCH = 7,             /* the kernel launch failed (cudaGetLastError) */
     ATTN_ERR_TIMEOUT = 8,            /* a bounded wait inside the kernel gave up */
     ATTN_ERR_CUDA = 9,               /* another CUDA runtime call failed */
-    ATTN_ERR_BAD_ARG = 10            /* causal not 0/1, or another malformed argument */
+    ATTN_ERR_BAD_ARG = 10,           /* causal not 0/1, or another malformed argument */
+    ATTN_ERR_TOO_LARGE = 11          /* the problem does not fit attn_fwd_host_noalloc's fixed scratch */
 } attn_status;
 
 /*
@@ -86,6 +87,35 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  */
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * attn_fwd_host_noalloc - attn_fwd_host for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call. attn_fwd_host stages the host
+ * arrays through device memory it allocates on every call; some callers cannot
+ * allocate at that point (another framework's caching allocator owns the
+ * device memory, or the thread must not take the implicit synchronisation an
+ * allocation can bring). This entry point computes the same result with no
+ * cudaMalloc, cudaMallocAsync or cudaFree: Q, K, V, O and LSE are staged
+ * through one fixed device array of ATTN_NOALLOC_SCRATCH_BYTES, held by every
+ * device the call has run on until the process exits.
+ *
+ *   arguments as for attn_fwd_host (host arrays, owned by the caller).
+ *
+ * Limit: 4 * round_up(B*H*N*d*2, 256) + round_up(B*H*N*4, 256) bytes must fit
+ * in ATTN_NOALLOC_SCRATCH_BYTES (e.g. B*H*N*d up to about 8M elements);
+ * larger problems return ATTN_ERR_TOO_LARGE before anything is copied.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * Every call shares the one array: calls whose work overlaps on the GPU (on
+ * different streams, or from different host threads) race and must be
+ * serialised by the caller. Nothing in the array needs clearing between calls:
+ * each call copies in every byte the kernel reads. Synchronises `stream`
+ * before returning, like attn_fwd_host.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
+int attn_fwd_host_noalloc(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                          int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
  * attn_device_status - failures that only the kernel can see.

@@ -31,15 +31,16 @@ def _declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     declared = _declared_functions()
-    assert set(declared) >= {"attn_fwd", "attn_fwd_host", "attn_device_status", "attn_set_wait_limit_ns",
-                             "attn_set_test_stall", "attn_status_string", "attn_abi_version"}
+    assert set(declared) >= {"attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
+                             "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string",
+                             "attn_abi_version"}
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in include/ but not exported"
     assert set(declared) == set(bos.EXPORTED_SYMBOLS)
 
 
 def test_status_strings(lib):
-    for code in range(0, 11):
+    for code in range(0, 12):
         s = bos.attn_status_string(code)
         assert s and s != "unknown status"
     assert bos.attn_status_string(12345) == "unknown status"
