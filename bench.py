@@ -35,7 +35,8 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 (bf16) and fraction of dense BF16 peak"
 UNIT = "TFLOP/s"
-KERNEL_SOURCES = ("blocked_online_softmax_gb300/csrc",)
+KERNEL_SOURCES = ("blocked_online_softmax_gb300/csrc/attn_fwd_sm103.cu",
+                  "blocked_online_softmax_gb300/csrc/sm103_ptx.cuh")
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -58,13 +59,11 @@ def dist_env():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the attention kernel's sources (the counters in profiles/ are tied to it)."""
     h = hashlib.sha256()
-    for d in KERNEL_SOURCES:
-        base = os.path.join(ROOT, d)
-        for name in sorted(os.listdir(base)):
-            if name.endswith((".cu", ".cuh", ".h")):
-                with open(os.path.join(base, name), "rb") as f:
-                    h.update(name.encode() + b"\0" + f.read())
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(os.path.basename(rel).encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

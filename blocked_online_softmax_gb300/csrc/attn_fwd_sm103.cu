@@ -14,10 +14,11 @@
 //    share every K/V tile. CTAs are persistent (one per SM) and walk a static
 //    list of units: for causal masking the list is heaviest-first over all heads
 //    and dealt to CTAs in snake order, which balances the triangle of work.
-//  * Warp roles (384 threads): warp 0 issues TMA loads (Q per unit, then K_j,
-//    V_j into a multi-stage ring); warp 1 issues tcgen05 MMAs from one thread;
-//    warp 2 owns the tensor-memory allocation; warpgroups 1 and 2 run the
-//    softmax of Q tile 0 and Q tile 1, one thread per query row.
+//  * Warp roles (384 threads): warpgroups 0 and 1 run the softmax of Q tile 0
+//    and Q tile 1, one thread per query row, with 208 registers each after a
+//    setmaxnreg split; warp 8 issues TMA loads (Q per unit, then K_j, V_j into
+//    a multi-stage ring); warp 9 owns the tensor-memory allocation and issues
+//    tcgen05 MMAs from one thread.
 //  * Tensor memory (512 columns x 128 lanes): S_t = Q_t K^T (fp32, 128 cols per
 //    tile), P_t (bf16, written over the first 64 columns of S_t) and O_t (fp32,
 //    d columns). O += P V takes P straight from tensor memory.
@@ -52,25 +53,45 @@ using namespace ptx;
 constexpr int kBM = 128;                  // query rows per Q tile (tensor-memory lanes)
 constexpr int kBN = 128;                  // keys per K/V tile
 constexpr int kUnitRows = 2 * kBM;        // query rows per work unit
+// warps 0-3: softmax of Q tile 0, warps 4-7: softmax of Q tile 1 (warp w reads
+// TMEM lanes 32*(w%4)..+31, so each warpgroup covers the 128 rows of its tile);
+// warpgroup 2: warp 8 TMA producer, warp 9 MMA issuer and TMEM owner.
+// Registers after launch (384 x 168): 128 x (208 + 208 + 88) = 64512.
 constexpr int kThreads = 384;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma0 = 9;         // MMA stream of Q tile 0; also owns TMEM allocation
+constexpr int kWarpMma1 = 10;        // MMA stream of Q tile 1
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 88;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
-constexpr uint32_t kTmemCols = 512;
-// tensor-memory column of S_t (P_t overlays its first 64 columns) and of O_t
-__host__ __device__ constexpr uint32_t tmem_s_col(int t) { return (uint32_t)t * 128u; }
-__host__ __device__ constexpr uint32_t tmem_o_col(int t) { return 256u + (uint32_t)t * 128u; }
+// Each Q tile has its own 256-column TMEM allocation: S at column 0 (P overlays
+// its first 64 columns as packed bf16), O at column 128. The tensor core keeps
+// MMAs of one issuing thread into one allocation in order, one at a time; two
+// allocations fed by two warps run concurrently, which is what lets 128-wide
+// MMAs reach the tensor core's full rate.
+constexpr uint32_t kTmemColsPerTile = 256;
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 128;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;         // 1 s
 
 template <int D>
 struct Cfg {
     static constexpr int kTileBytes = kBN * D * 2;          // one bf16 Q, K or V tile
-    static constexpr int kStages = (D == 128) ? 4 : 8;      // K/V ring depth
+    // K/V ring depth. Three stages keep stream 0 at most about half a block ahead
+    // of stream 1 (measured faster than four on the causal workloads), and with
+    // three stages K_{i+2} reuses V_i's stage, which keeps stream 1's wait for
+    // S_0(i) free of phase aliasing (see mma_issuer).
+    static constexpr int kStages = 3;
     static constexpr int kBoxes = D / 64;                   // 64-column TMA boxes per tile
     static constexpr int kOffKV = 2 * kTileBytes;           // after the two Q tiles
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-    // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain, never
-    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1 + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
+    // barriers: q_full, q_empty, kv_full[S], kv_empty[S], then per Q tile s_full[2], p_half[2],
+    // p_full[2], o_full[2], drain[2], then never (test hook), then s0_done[2] (S_0(i) complete,
+    // slot i & 1, for stream 1)
+    static constexpr int kBarTile = 2 + 2 * kStages;
+    static constexpr int kNumBars = kBarTile + 10 + 1 + 2;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slots [2], abort flag
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 };
 
@@ -90,15 +111,19 @@ __device__ int g_attn_device_status;
 
 namespace {
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted. The
+// waiting thread sleeps inside try_wait (up to ~0.5 ms per try) instead of
+// spinning, so waiting warps leave the issue slots to the softmax warps that
+// share their SM sub-partition.
+constexpr uint32_t kSuspendNs = 500000;
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                               volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = (uint32_t)(limit_ns < kSuspendNs ? limit_ns : kSuspendNs);
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
@@ -209,120 +234,242 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     if (q_parity >= 0) mbar_wait(q_full, (uint32_t)q_parity, kDrainLimitNs);
 }
 
+// S_t = Q_t K^T into the tile's TMEM allocation `tm`.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tmem, int t, const uint8_t* sQ, const uint8_t* sK) {
-    using C = Cfg<D>;
+__device__ __forceinline__ void issue_s(uint32_t tm, const uint8_t* sQt, const uint8_t* sK) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, false);
-    const uint32_t qa = smem_u32(sQ + t * C::kTileBytes), ka = smem_u32(sK);
+    const uint32_t qa = smem_u32(sQt), ka = smem_u32(sK);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;   // 64-column box, 32-byte K step
-        mma_ss(tmem + tmem_s_col(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc,
+        mma_ss(tm + kTmemS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc,
                kk > 0 ? 1u : 0u);
     }
 }
 
+// O_t (+)= P_t[:, keys of steps kk0..kk1) * V[those keys, :], in the tile's allocation `tm`.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, int t, const uint8_t* sV, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tm, const uint8_t* sV, bool accumulate, int kk0, int kk1) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
     const uint32_t va = smem_u32(sV);
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk)   // 16 keys per step: 8 P columns, 16 V rows (2048 bytes)
-        mma_ts(tmem + tmem_o_col(t), tmem + tmem_s_col(t) + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), idesc,
+    for (int kk = kk0; kk < kk1; ++kk)   // 16 keys per step: 8 P columns, 16 V rows (2048 bytes)
+        mma_ts(tm + kTmemO, tm + kTmemS + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), idesc,
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
+
+
+// One MMA stream: Q tile t's S_t = Q_t K^T and O_t += P_t V, issued by one
+// thread, in the order S(i), PV(i), S(i+1), ... (S(i+1) overwrites P(i), which
+// in-order execution within the stream makes safe). Both streams walk the same
+// K/V ring; a stage is free once both have committed it.
+//
+// The streams are kept half a block apart: stream 1 issues S_1(i) only once
+// S_0(i) has completed, so S_1(i) runs while softmax 0 works on S_0(i), PV_0(i)
+// runs while softmax 1 works on S_1(i), and the two softmax warpgroups rarely
+// compete for the exp2 unit. Stream 0 signals "S_0(i) complete" on barrier
+// s0_done[i & 1]. Stream 1's wait for that signal cannot alias the next one on
+// the same barrier (S_0(i+2)): S_0(i+2) needs K_{i+2}, whose stage (with three
+// stages) is V_i's, freed only after PV_1(i) completes, and stream 1 issues
+// PV_1(i) only after this wait. Nothing in stream 0 waits on stream 1 other than
+// through the ring and the Q buffer, so the order cannot deadlock.
 template <int D>
-__device__ void mma_issuer(uint32_t tmem, const uint8_t* sQ, const uint8_t* sKV, uint64_t* bars,
+__device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sKV, uint64_t* bars,
                            volatile int* abort_flag, const KernelArgs& a) {
     using C = Cfg<D>;
     uint64_t* q_full = bars + 0;
     uint64_t* q_empty = bars + 1;
     uint64_t* kv_full = bars + 2;
     uint64_t* kv_empty = bars + 2 + C::kStages;
-    uint64_t* s_full = bars + 2 + 2 * C::kStages;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* o_full = p_full + 2;
-    uint64_t* drain = o_full + 2;
-    uint64_t* never = o_full + 3;
+    uint64_t* s_full = bars + C::kBarTile;
+    uint64_t* p_half = s_full + 2;
+    uint64_t* p_full = s_full + 4;
+    uint64_t* o_full = s_full + 6;
+    uint64_t* drain = s_full + 8;      // drain[2]
+    uint64_t* never = s_full + 10;
+    uint64_t* s0_done = s_full + 11;   // [2]
     const uint64_t lim = a.wait_limit_ns;
     const int total = a.BH * a.U;
+    const uint8_t* sQt = sQ + t * C::kTileBytes;
     int stage = 0;
-    uint32_t phase = 0;
-    uint32_t p_phase[2] = {0, 0};
+    uint32_t phase = 0, p_phase = 0;
+    uint32_t s0_count = 0;             // S_0 blocks signalled (stream 0) or awaited (stream 1) so far
     bool ok = true;
-    auto next_stage = [&](int& st) -> bool {
-        st = stage;
-        const bool got = wait_or_abort(&kv_full[stage], phase, lim, abort_flag);
-        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-        return got;
-    };
-    if (a.test_stall && !wait_or_abort(never, 0, lim, abort_flag)) ok = false;
+    if (t == 0 && a.test_stall && !wait_or_abort(never, 0, lim, abort_flag)) ok = false;
     int it = 0;
     for (int r = 0; ok; ++r, ++it) {
         const int k = unit_index(r);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
+        const int first = (t == 0) ? u.first0 : 0;
         if (!wait_or_abort(q_full, it & 1, lim, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        int kst, vst;
-        if (!next_stage(kst)) { ok = false; break; }
-        tc_fence_after();
-        const uint8_t* sK = sKV + kst * C::kTileBytes;
-        if (u.first0 == 0) { issue_s<D>(tmem, 0, sQ, sK); mma_commit(&s_full[0]); }
-        issue_s<D>(tmem, 1, sQ, sK);
-        mma_commit(&s_full[1]);
-        mma_commit(&kv_empty[kst]);
-        if (u.n == 1) mma_commit(q_empty);
         for (int i = 0; i < u.n; ++i) {
-            if (!next_stage(vst)) { ok = false; break; }
-            const uint8_t* sV = sKV + vst * C::kTileBytes;
-            if (i >= u.first0) {
-                if (!wait_or_abort(&p_full[0], p_phase[0], lim, abort_flag)) { ok = false; break; }
-                p_phase[0] ^= 1;
-                tc_fence_after();
-                issue_pv<D>(tmem, 0, sV, i > u.first0);
-                if (i == u.n - 1) mma_commit(&o_full[0]);
+            const bool active = (i >= first);
+            const int kst = stage;
+            if (!wait_or_abort(&kv_full[stage], phase, lim, abort_flag)) { ok = false; break; }
+            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            if (t == 1 && i >= u.first0) {          // tile 0 is active in this block
+                if (!wait_or_abort(&s0_done[s0_count & 1], (s0_count >> 1) & 1, lim, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++s0_count;
             }
-            const bool more = (i + 1 < u.n);
-            if (more) {
-                if (!next_stage(kst)) { ok = false; break; }
+            if (active) {
                 tc_fence_after();
-                sK = sKV + kst * C::kTileBytes;
-                if (i + 1 >= u.first0) { issue_s<D>(tmem, 0, sQ, sK); mma_commit(&s_full[0]); }
+                issue_s<D>(tm, sQt, sKV + kst * C::kTileBytes);
+                mma_commit(&s_full[t]);
+                if (t == 0) {
+                    mma_commit(&s0_done[s0_count & 1]);
+                    ++s0_count;
+                }
             }
-            if (!wait_or_abort(&p_full[1], p_phase[1], lim, abort_flag)) { ok = false; break; }
-            p_phase[1] ^= 1;
-            tc_fence_after();
-            issue_pv<D>(tmem, 1, sV, i > 0);
+            mma_commit(&kv_empty[kst]);
+            if (i == u.n - 1) mma_commit(q_empty);
+            const int vst = stage;
+            if (!wait_or_abort(&kv_full[stage], phase, lim, abort_flag)) { ok = false; break; }
+            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            if (active) {
+                const uint8_t* sV = sKV + vst * C::kTileBytes;
+                // each 64-key half of P_t as soon as the softmax has written it
+                if (!wait_or_abort(&p_half[t], p_phase, lim, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv<D>(tm, sV, i > first, 0, kBN / 32);
+                if (!wait_or_abort(&p_full[t], p_phase, lim, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv<D>(tm, sV, true, kBN / 32, kBN / 16);
+                p_phase ^= 1;
+                if (i == u.n - 1) mma_commit(&o_full[t]);
+            }
             mma_commit(&kv_empty[vst]);
-            if (i == u.n - 1) mma_commit(&o_full[1]);
-            if (more) {
-                issue_s<D>(tmem, 1, sQ, sK);
-                mma_commit(&s_full[1]);
-                mma_commit(&kv_empty[kst]);
-                if (i + 1 == u.n - 1) mma_commit(q_empty);
-            }
         }
     }
     // Every MMA this thread issued must complete before tensor memory is freed.
-    mma_commit(drain);
-    mbar_wait(drain, 0, kDrainLimitNs);
+    mma_commit(&drain[t]);
+    mbar_wait(&drain[t], 0, kDrainLimitNs);
+}
+
+// Packed fp32 pair helpers (sm_100 family: one instruction for two lanes of work).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Running max (kMax) or min of 32 raw scores into 8 chains.
+template <bool kMax>
+__device__ __forceinline__ void chunk_extreme(const uint32_t* x, float (&m)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float a = __uint_as_float(x[q]), b = __uint_as_float(x[q + 8]);
+        const float cc = __uint_as_float(x[q + 16]), d = __uint_as_float(x[q + 24]);
+        m[q] = kMax ? max3(m[q], max3(a, b, cc), d) : min3(m[q], min3(a, b, cc), d);
+    }
+}
+
+template <bool kMax>
+__device__ __forceinline__ float reduce8(const float (&m)[8]) {
+    const float a = kMax ? max3(m[0], m[1], m[2]) : min3(m[0], m[1], m[2]);
+    const float b = kMax ? max3(m[3], m[4], m[5]) : min3(m[3], m[4], m[5]);
+    return kMax ? max3(a, b, fmaxf(m[6], m[7])) : min3(a, b, fminf(m[6], m[7]));
+}
+
+// Row max (scale c >= 0) or row min (c < 0) of 128 raw scores, 8 chains deep.
+template <bool kMax>
+__device__ __forceinline__ float row_extreme(const uint32_t (&sr)[128]) {
+    float m[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m[q] = kMax ? -INFINITY : INFINITY;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) chunk_extreme<kMax>(&sr[ch * 32], m);
+    return reduce8<kMax>(m);
+}
+
+// Max over the first `lim` columns of the scaled scores s * c (keys past a
+// row's last valid key are masked out), 8 chains deep.
+__device__ __forceinline__ float masked_row_max(const uint32_t (&sr)[128], float c, int lim) {
+    float m[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m[q] = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 128; cc += 8) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float x = __uint_as_float(sr[cc + q]) * c;
+            m[q] = fmaxf(m[q], (cc + q < lim) ? x : -INFINITY);
+        }
+    }
+    return fmaxf(max3(m[0], m[1], m[2]), max3(m[3], m[4], fmaxf(m[5], fmaxf(m[6], m[7]))));
+}
+
+// exp2 of 32 scores (keys 32*ch .. 32*ch+31): x = s * c - m in one packed FMA per
+// pair, p = 2^x (0 for columns >= lim when kMasked), written to P_t as 16 packed
+// bf16 pairs; the fp32 probabilities are added pairwise into acc[4].
+template <bool kMasked>
+__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[128], int ch, uint64_t c2, uint64_t negm2,
+                                          uint64_t (&acc)[4], uint32_t tS, int lim) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int c0 = ch * 32 + 2 * e;
+        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), c2, negm2);
+        float x0, x1;
+        f2_unpack(x2, x0, x1);
+        float p0 = ex2(x0), p1 = ex2(x1);
+        if (kMasked) {
+            p0 = (c0 < lim) ? p0 : 0.f;
+            p1 = (c0 + 1 < lim) ? p1 : 0.f;
+        }
+        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+        pk[e] = pack_bf16(p0, p1);
+    }
+    tmem_st16(tS + ch * 16, pk);
 }
 
 template <int D>
-__device__ void softmax_role(uint32_t tmem, int t, int wq, int lane, uint64_t* bars, volatile int* abort_flag,
+__device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, volatile int* abort_flag,
                              const KernelArgs& a) {
     using C = Cfg<D>;
-    uint64_t* s_full = bars + 2 + 2 * C::kStages;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* o_full = p_full + 2;
+    uint64_t* s_full = bars + C::kBarTile;
+    uint64_t* p_half = s_full + 2;
+    uint64_t* p_full = s_full + 4;
+    uint64_t* o_full = s_full + 6;
     const uint64_t lim = a.wait_limit_ns;
-    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const uint32_t tS = lane_base + tmem_s_col(t);
-    const uint32_t tO = lane_base + tmem_o_col(t);
+    const uint32_t lane_base = tm + ((uint32_t)(wq * 32) << 16);
+    const uint32_t tS = lane_base + kTmemS;
+    const uint32_t tO = lane_base + kTmemO;
     const int row_in_tile = wq * 32 + lane;
     const float c = a.scale_log2;
+    const uint64_t c2 = f2_pack(c, c);
     const int total = a.BH * a.U;
     uint32_t s_phase = 0, o_phase = 0;
     bool ok = true;
@@ -343,35 +490,23 @@ __device__ void softmax_role(uint32_t tmem, int t, int wq, int lane, uint64_t* b
             s_phase ^= 1;
             tc_fence_after();
             uint32_t sr[128];
-            tmem_ld128(tS, sr);
             const int key0 = j * kBN;
             const bool need_mask = (key0 + kBN > a.N) || (a.causal && key0 + kBN - 1 > tile_row0);
+            // valid keys of this row in this block: key < N and, causal, key <= row
+            int lim = kBN;
             float m_tile;
             if (need_mask) {
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int cc = 0; cc < 128; ++cc) {
-                    const int key = key0 + cc;
-                    float x = __uint_as_float(sr[cc]) * c;
-                    if (key >= a.N || (a.causal && key > row)) x = -INFINITY;
-                    sr[cc] = __float_as_uint(x);
-                    mx[cc & 3] = fmaxf(mx[cc & 3], x);
-                }
-                m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                const int last = a.causal ? min(a.N, row + 1) : a.N;
+                lim = max(0, min(kBN, last - key0));
+                tmem_ld128(tS, sr);
+                m_tile = masked_row_max(sr, c, lim);
             } else {
-                float mx[4], mn[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) mx[q] = mn[q] = __uint_as_float(sr[q]);
-#pragma unroll
-                for (int cc = 4; cc < 128; ++cc) {
-                    const float s = __uint_as_float(sr[cc]);
-                    mx[cc & 3] = fmaxf(mx[cc & 3], s);
-                    mn[cc & 3] = fminf(mn[cc & 3], s);
-                }
-                const float smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                const float smin = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
-                m_tile = (c >= 0.f) ? smax * c : smin * c;
+                tmem_ld128(tS, sr);
+                m_tile = (c >= 0.f) ? row_extreme<true>(sr) * c : row_extreme<false>(sr) * c;
             }
+            // Move the reference max only when the block's max exceeds it by more
+            // than 2^8; then rescale O_t (complete up to the previous block: the
+            // commit behind s_full covers every earlier MMA) and l.
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 m_ref = m_tile;
@@ -379,29 +514,6 @@ __device__ void softmax_role(uint32_t tmem, int t, int wq, int lane, uint64_t* b
                 alpha = ex2(m_ref - m_tile);
                 m_ref = m_tile;
             }
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {           // 32 keys -> 16 packed bf16 pairs per chunk
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c0 = ch * 32 + 2 * e;
-                    float p0, p1;
-                    if (need_mask) {
-                        p0 = ex2(__uint_as_float(sr[c0]) - m_use);
-                        p1 = ex2(__uint_as_float(sr[c0 + 1]) - m_use);
-                    } else {
-                        p0 = ex2(fmaf(__uint_as_float(sr[c0]), c, -m_use));
-                        p1 = ex2(fmaf(__uint_as_float(sr[c0 + 1]), c, -m_use));
-                    }
-                    sum[e & 3] += p0;
-                    sum[(e + 2) & 3] += p1;
-                    pk[e] = pack_bf16(p0, p1);
-                }
-                tmem_st16(tS + ch * 16, pk);
-            }
-            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
@@ -412,9 +524,34 @@ __device__ void softmax_role(uint32_t tmem, int t, int wq, int lane, uint64_t* b
                     tmem_st32(tO + ch * 32, orow);
                 }
             }
+            const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const uint64_t negm2 = f2_pack(negm, negm);
+            uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
+            // first 64 keys: hand P's first half to the MMA as soon as it is in TMEM
+            if (need_mask) {
+                exp_chunk<true>(sr, 0, c2, negm2, acc, tS, lim);
+                exp_chunk<true>(sr, 1, c2, negm2, acc, tS, lim);
+            } else {
+                exp_chunk<false>(sr, 0, c2, negm2, acc, tS, lim);
+                exp_chunk<false>(sr, 1, c2, negm2, acc, tS, lim);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_half[t]);
+            if (need_mask) {
+                exp_chunk<true>(sr, 2, c2, negm2, acc, tS, lim);
+                exp_chunk<true>(sr, 3, c2, negm2, acc, tS, lim);
+            } else {
+                exp_chunk<false>(sr, 2, c2, negm2, acc, tS, lim);
+                exp_chunk<false>(sr, 3, c2, negm2, acc, tS, lim);
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[t]);
+            const uint64_t s01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+            float sum0, sum1;
+            f2_unpack(s01, sum0, sum1);
+            l = l * alpha + (sum0 + sum1);
         }
         if (!ok) break;
         // epilogue: O / l -> bf16, LSE in natural log
@@ -458,56 +595,69 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + C::kOffKV;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [2]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
         mbar_init(bars + 0, 1);                                  // q_full
-        mbar_init(bars + 1, 1);                                  // q_empty
+        mbar_init(bars + 1, 2);                                  // q_empty: one commit per MMA stream
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bars + 2 + s, 1);                          // kv_full
-            mbar_init(bars + 2 + C::kStages + s, 1);             // kv_empty
+            mbar_init(bars + 2 + C::kStages + s, 2);             // kv_empty: one commit per MMA stream
         }
-        uint64_t* s_full = bars + 2 + 2 * C::kStages;
+        uint64_t* s_full = bars + C::kBarTile;
         for (int t = 0; t < 2; ++t) {
-            mbar_init(s_full + t, 1);                            // s_full
-            mbar_init(s_full + 2 + t, kBM);                      // p_full: every softmax thread arrives
-            mbar_init(s_full + 4 + t, 1);                        // o_full
+            mbar_init(s_full + t, 1);                            // s_full: MMA commit
+            mbar_init(s_full + 2 + t, kBM);                      // p_half: every softmax thread arrives
+            mbar_init(s_full + 4 + t, kBM);                      // p_full: every softmax thread arrives
+            mbar_init(s_full + 6 + t, 1);                        // o_full: MMA commit
         }
-        mbar_init(s_full + 6, 1);                                // drain
-        mbar_init(s_full + 7, 1);                                // never (test hook)
+        mbar_init(s_full + 8, 1);                                // drain, stream 0
+        mbar_init(s_full + 9, 1);                                // drain, stream 1
+        mbar_init(s_full + 10, 1);                               // never (test hook)
+        mbar_init(s_full + 11, 1);                               // s0_done[0]
+        mbar_init(s_full + 12, 1);                               // s0_done[1]
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == kWarpProducer && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
-    if (warp == 2) {
-        tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kWarpMma0) {
+        tmem_alloc(tmem_slot, kTmemColsPerTile);
+        tmem_alloc(tmem_slot + 1, kTmemColsPerTile);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem0 = tmem_slot[0], tmem1 = tmem_slot[1];
 
-    if (warp == 0) {
-        if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, abort_flag, a);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) mma_issuer<D>(tmem, sQ, sKV, bars, abort_flag, a);
-        __syncwarp();
-    } else if (warp >= 4) {
-        softmax_role<D>(tmem, (warp - 4) / 4, warp % 4, lane, bars, abort_flag, a);
+    if (warp < kWarpProducer) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, abort_flag, a);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+        if (warp == kWarpProducer) {
+            if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, abort_flag, a);
+            __syncwarp();
+        } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+            const int t = warp - kWarpMma0;
+            if (lane == 0) mma_issuer<D>(t ? tmem1 : tmem0, t, sQ, sKV, bars, abort_flag, a);
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kWarpMma0) {
+        tmem_dealloc(tmem0, kTmemColsPerTile);
+        tmem_dealloc(tmem1, kTmemColsPerTile);
+    }
 }
 
 // ------------------------------------------------------------------ host side

@@ -61,6 +61,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same test, but the thread may be suspended (not spinning, so it takes no
+// issue slots from other warps) until the phase completes or about
+// `suspend_ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete. Gives up after
 // `limit_ns` nanoseconds of wall time and returns false; never spins forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -287,6 +302,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         BOS_W8(0), BOS_W8(8), BOS_W8(16), BOS_W8(24)
         : "memory");
 }
+
+// 32 columns without waiting; pair with tmem_ld_wait32 on the same registers
+// before reading them (the wait names the registers, so the compiler cannot
+// read them earlier).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        : BOS_R8(0), BOS_R8(8), BOS_R8(16), BOS_R8(24)
+        : "r"(taddr)
+        : "memory");
+}
+
+#define BOS_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                   "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+
+// Waits for this thread's outstanding tcgen05.ld; the 32 registers it names
+// become readable after it.
+__device__ __forceinline__ void tmem_ld_wait32(uint32_t* r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" : BOS_RW8(0), BOS_RW8(8), BOS_RW8(16), BOS_RW8(24) :: "memory");
+}
+
+#undef BOS_RW8
 
 // Wait until this thread's earlier tcgen05.st have completed.
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
