@@ -84,13 +84,15 @@ struct Cfg {
     // S_0(i) free of phase aliasing (see mma_issuer).
     static constexpr int kStages = 3;
     static constexpr int kBoxes = D / 64;                   // 64-column TMA boxes per tile
-    static constexpr int kOffKV = 2 * kTileBytes;           // after the two Q tiles
+    // Q is double-buffered (2 buffers x 2 tiles): the next unit's Q tiles load
+    // while the current unit runs, so a unit starts as soon as its K_0 lands.
+    static constexpr int kOffKV = 4 * kTileBytes;
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-    // barriers: q_full, q_empty, kv_full[S], kv_empty[S], then per Q tile s_full[2], p_half[2],
+    // barriers: q_full[2], q_empty[2] (per Q buffer), kv_full[S], kv_empty[S], then per Q tile s_full[2], p_half[2],
     // p_full[2], o_full[2], drain[2], then never (test hook), then s0_done[2] (S_0(i) complete,
-    // slot i & 1, for stream 1)
-    static constexpr int kBarTile = 2 + 2 * kStages;
-    static constexpr int kNumBars = kBarTile + 10 + 1 + 2;
+    // slot i & 1, for stream 1), then o_staged[2] (a warpgroup's O tile is in shared memory)
+    static constexpr int kBarTile = 4 + 2 * kStages;
+    static constexpr int kNumBars = kBarTile + 10 + 1 + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slots [2], abort flag
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 };
@@ -184,16 +186,16 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
                          uint8_t* sQ, uint8_t* sKV, uint64_t* bars, volatile int* abort_flag,
                          const KernelArgs& a) {
     using C = Cfg<D>;
-    uint64_t* q_full = bars + 0;
-    uint64_t* q_empty = bars + 1;
-    uint64_t* kv_full = bars + 2;
-    uint64_t* kv_empty = bars + 2 + C::kStages;
+    uint64_t* q_full = bars + 0;      // [2]
+    uint64_t* q_empty = bars + 2;     // [2]
+    uint64_t* kv_full = bars + 4;
+    uint64_t* kv_empty = bars + 4 + C::kStages;
     const int total = a.BH * a.U;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0;             // stages with a load whose completion is not yet observed
     uint32_t issued_parity = 0;           // parity of that load's phase, per stage
-    int q_parity = -1;                    // parity of the last Q load's phase, -1 before the first
+    int q_parity[2] = {-1, -1};           // per Q buffer: parity of its last load's phase, -1 before any
     bool ok = true;
     // One K/V tile into the next ring stage.
     auto load_kv = [&](const CUtensorMap* tm, int j, int bh) -> bool {
@@ -211,27 +213,27 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         const int k = unit_index(r);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
-        // The first K/V pair of a unit goes ahead of its Q tiles: Q must wait until the
-        // previous unit's last S = Q K^T has read the Q buffer, the ring need not.
+        // Q tiles first (their buffer was released by the unit before last), then
+        // the unit's K/V stream.
+        const int qb = it & 1;
+        if (!wait_or_abort(&q_empty[qb], ((it >> 1) & 1) ^ 1, a.wait_limit_ns, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(&q_full[qb], 2 * C::kTileBytes);
+        q_parity[qb] = (it >> 1) & 1;
+        for (int t = 0; t < 2; ++t)
+            for (int b = 0; b < C::kBoxes; ++b)
+                tma_load_3d(sQ + (qb * 2 + t) * C::kTileBytes + b * 16384, tm_q, &q_full[qb], b * 64,
+                            u.row0 + t * kBM, u.bh);
         for (int i = 0; i < u.n && ok; ++i) {
             const int j = u.n - 1 - i;
             if (!load_kv(tm_k, j, u.bh) || !load_kv(tm_v, j, u.bh)) { ok = false; break; }
-            if (i == 0) {
-                if (!wait_or_abort(q_empty, (it & 1) ^ 1, a.wait_limit_ns, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
-                q_parity = it & 1;
-                for (int t = 0; t < 2; ++t)
-                    for (int b = 0; b < C::kBoxes; ++b)
-                        tma_load_3d(sQ + t * C::kTileBytes + b * 16384, tm_q, q_full, b * 64, u.row0 + t * kBM,
-                                    u.bh);
-            }
         }
     }
     // Every copy this thread started must land before the CTA may exit (on the
     // normal path they already have).
     for (int s = 0; s < C::kStages; ++s)
         if (issued_mask & (1u << s)) mbar_wait(&kv_full[s], (issued_parity >> s) & 1u, kDrainLimitNs);
-    if (q_parity >= 0) mbar_wait(q_full, (uint32_t)q_parity, kDrainLimitNs);
+    for (int qb = 0; qb < 2; ++qb)
+        if (q_parity[qb] >= 0) mbar_wait(&q_full[qb], (uint32_t)q_parity[qb], kDrainLimitNs);
 }
 
 // S_t = Q_t K^T into the tile's TMEM allocation `tm`.
@@ -278,10 +280,10 @@ template <int D>
 __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sKV, uint64_t* bars,
                            volatile int* abort_flag, const KernelArgs& a) {
     using C = Cfg<D>;
-    uint64_t* q_full = bars + 0;
-    uint64_t* q_empty = bars + 1;
-    uint64_t* kv_full = bars + 2;
-    uint64_t* kv_empty = bars + 2 + C::kStages;
+    uint64_t* q_full = bars + 0;      // [2]
+    uint64_t* q_empty = bars + 2;     // [2]
+    uint64_t* kv_full = bars + 4;
+    uint64_t* kv_empty = bars + 4 + C::kStages;
     uint64_t* s_full = bars + C::kBarTile;
     uint64_t* p_half = s_full + 2;
     uint64_t* p_full = s_full + 4;
@@ -291,7 +293,6 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
     uint64_t* s0_done = s_full + 11;   // [2]
     const uint64_t lim = a.wait_limit_ns;
     const int total = a.BH * a.U;
-    const uint8_t* sQt = sQ + t * C::kTileBytes;
     int stage = 0;
     uint32_t phase = 0, p_phase = 0;
     uint32_t s0_count = 0;             // S_0 blocks signalled (stream 0) or awaited (stream 1) so far
@@ -303,7 +304,9 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
         const int first = (t == 0) ? u.first0 : 0;
-        if (!wait_or_abort(q_full, it & 1, lim, abort_flag)) { ok = false; break; }
+        const int qb = it & 1;
+        const uint8_t* sQt = sQ + (qb * 2 + t) * C::kTileBytes;
+        if (!wait_or_abort(&q_full[qb], (it >> 1) & 1, lim, abort_flag)) { ok = false; break; }
         for (int i = 0; i < u.n; ++i) {
             const bool active = (i >= first);
             const int kst = stage;
@@ -326,7 +329,7 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
                 }
             }
             mma_commit(&kv_empty[kst]);
-            if (i == u.n - 1) mma_commit(q_empty);
+            if (i == u.n - 1) mma_commit(&q_empty[qb]);
             const int vst = stage;
             if (!wait_or_abort(&kv_full[stage], phase, lim, abort_flag)) { ok = false; break; }
             if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -455,14 +458,21 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[128], int ch, uin
     tmem_st16(tS + ch * 16, pk);
 }
 
+// Softmax warpgroup of Q tile t (thread = query row = TMEM lane). After a unit's
+// last block it also writes the unit's O tile: O / l as bf16 into the unit's own
+// Q_t buffer (free once PV_t of the last block is done) in the 128-byte-swizzled
+// layout, then one thread stores it with TMA (rows past N are clipped) and
+// releases the Q buffer once the store has read it.
 template <int D>
 __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, volatile int* abort_flag,
-                             const KernelArgs& a) {
+                             uint8_t* sQ, const CUtensorMap* tm_o, const KernelArgs& a) {
     using C = Cfg<D>;
+    uint64_t* q_empty = bars + 2;     // [2]
     uint64_t* s_full = bars + C::kBarTile;
     uint64_t* p_half = s_full + 2;
     uint64_t* p_full = s_full + 4;
     uint64_t* o_full = s_full + 6;
+    uint64_t* o_staged = s_full + 13;  // [2]
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t lane_base = tm + ((uint32_t)(wq * 32) << 16);
     const uint32_t tS = lane_base + kTmemS;
@@ -554,7 +564,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             l = l * alpha + (sum0 + sum1);
         }
         if (!ok) break;
-        // epilogue: O / l -> bf16, LSE in natural log
+        // epilogue: O / l -> bf16 through shared memory and TMA, LSE in natural log
         bool got = wait_or_abort(&o_full[t], o_phase, lim, abort_flag);
         got = __all_sync(0xffffffffu, got);
         if (!got) { ok = false; break; }
@@ -562,25 +572,46 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         tc_fence_after();
         const float l_safe = (l > 0.f) ? l : 1.f;
         const float inv = 1.f / l_safe;
-        __nv_bfloat16* orow_ptr = a.o + ((int64_t)u.bh * a.N + row) * D;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t ov[32];
-            tmem_ld32(tO + ch * 32, ov);
-            uint32_t pk[16];
+        uint32_t ov[D];
+        if constexpr (D == 128) {
+            tmem_ld128(tO, ov);
+        } else {
+            uint32_t (&h0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[0]);
+            uint32_t (&h1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[32]);
+            tmem_ld32(tO, h0);
+            tmem_ld32(tO + 32, h1);
+        }
+        const int qb = r & 1;
+        uint8_t* stage = sQ + (qb * 2 + t) * C::kTileBytes;
+        uint8_t* srow = stage + row_in_tile * 128;
+        const int swz = row_in_tile & 7;
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-            if (row < a.N) {
-                uint4* dst = reinterpret_cast<uint4*>(orow_ptr + ch * 32);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        for (int c16 = 0; c16 < D / 8; ++c16) {     // 16-byte chunk = 8 output columns
+            const int col = c16 * 8;
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
+            // 64-column box (c16 / 8), 128-byte swizzle: chunk index XOR (row & 7)
+            *reinterpret_cast<uint4*>(srow + (c16 >> 3) * 16384 + (((c16 & 7) ^ swz) << 4)) = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&o_staged[t]);
+        if (row_in_tile == 0) {
+            // a bounded wait, so a warp that aborted cannot leave this thread stuck
+            if (wait_or_abort(&o_staged[t], o_phase ^ 1, lim, abort_flag)) {
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_store_3d(tm_o, stage + b * 16384, b * 64, tile_row0, u.bh);
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(&q_empty[qb]);
             }
         }
         if (row < a.N) a.lse[(int64_t)u.bh * a.N + row] = (m_ref + log2f(l_safe)) * 0.69314718055994531f;
         tc_fence_before();
     }
+    if (row_in_tile == 0) bulk_wait0();   // this warpgroup's O stores are complete
 }
 
 // ------------------------------------------------------------------ kernel
@@ -588,7 +619,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const KernelArgs a) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const KernelArgs a) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -600,11 +632,14 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(bars + 0, 1);                                  // q_full
-        mbar_init(bars + 1, 2);                                  // q_empty: one commit per MMA stream
+        for (int qb = 0; qb < 2; ++qb) {
+            mbar_init(bars + qb, 1);                             // q_full[qb]
+            mbar_init(bars + 2 + qb, 4);                         // q_empty[qb]: a commit per MMA stream, an
+                                                                 // arrival per softmax warpgroup (O stored)
+        }
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bars + 2 + s, 1);                          // kv_full
-            mbar_init(bars + 2 + C::kStages + s, 2);             // kv_empty: one commit per MMA stream
+            mbar_init(bars + 4 + s, 1);                          // kv_full
+            mbar_init(bars + 4 + C::kStages + s, 2);             // kv_empty: one commit per MMA stream
         }
         uint64_t* s_full = bars + C::kBarTile;
         for (int t = 0; t < 2; ++t) {
@@ -618,6 +653,8 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_init(s_full + 10, 1);                               // never (test hook)
         mbar_init(s_full + 11, 1);                               // s0_done[0]
         mbar_init(s_full + 12, 1);                               // s0_done[1]
+        mbar_init(s_full + 13, kBM);                             // o_staged[0]: every softmax thread arrives
+        mbar_init(s_full + 14, kBM);                             // o_staged[1]
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -625,6 +662,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_o);
     }
     if (warp == kWarpMma0) {
         tmem_alloc(tmem_slot, kTmemColsPerTile);
@@ -638,7 +676,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
     if (warp < kWarpProducer) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, abort_flag, a);
+        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, abort_flag, sQ, &tm_o, a);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
@@ -683,7 +721,7 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); 64x128 boxes, 128-byte
-// swizzle; rows past N read as zero.
+// swizzle; loads read rows past N as zero, stores drop them.
 bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH, int N, int D) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
@@ -703,9 +741,9 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return ATTN_ERR_CUDA;
     const int BH = p.B * p.H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, D) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, D) ||
-        !encode_qkv_map(enc, &mv, p.v, BH, p.N, D))
+        !encode_qkv_map(enc, &mv, p.v, BH, p.N, D) || !encode_qkv_map(enc, &mo, p.o, BH, p.N, D))
         return ATTN_ERR_BAD_SHAPE;
     static int sms_cache[64] = {0};
     static int attr_done[64] = {0};
@@ -737,7 +775,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.test_stall = g_test_stall;
     const int64_t units = (int64_t)BH * a.U;
     const int grid = (int)(units < sms ? units : sms);
-    attn_fwd_sm103_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
+    attn_fwd_sm103_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
