@@ -91,38 +91,11 @@ extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, 
     int dev = 0;
     st = check_device(&dev);
     if (st != ATTN_OK) return st;
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    const size_t elems = (size_t)B * H * N * d;
-    const size_t tbytes = elems * 2;                      // bf16
-    const size_t lbytes = (size_t)B * H * N * sizeof(float);
-    // One staging block: Q | K | V | O | LSE, each sub-buffer 256-byte aligned.
-    auto round_up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    const size_t off_k = round_up(tbytes), off_v = off_k + round_up(tbytes),
-                 off_o = off_v + round_up(tbytes), off_l = off_o + round_up(tbytes),
-                 total = off_l + round_up(lbytes);
-    char* base = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&base), total, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return ATTN_ERR_CUDA;
-    }
-    int rc = ATTN_OK;
-    if (cudaMemcpyAsync(base, q_h, tbytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(base + off_k, k_h, tbytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(base + off_v, v_h, tbytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
-        rc = ATTN_ERR_CUDA;
-    }
-    if (rc == ATTN_OK)
-        rc = attn_fwd(base, base + off_k, base + off_v, base + off_o,
-                      reinterpret_cast<float*>(base + off_l), B, H, N, d, scale, causal, stream);
-    if (rc == ATTN_OK &&
-        (cudaMemcpyAsync(o_h, base + off_o, tbytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-         cudaMemcpyAsync(lse_h, base + off_l, lbytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)) {
-        rc = ATTN_ERR_CUDA;
-    }
-    cudaFreeAsync(base, stream);
-    if (cudaStreamSynchronize(stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
-    if (rc != ATTN_OK) cudaGetLastError();
-    return rc;
+    bos::AttnParams p;
+    p.q = q_h; p.k = k_h; p.v = v_h; p.o = o_h; p.lse = lse_h;
+    p.B = B; p.H = H; p.N = N; p.d = d;
+    p.scale = scale; p.causal = causal;
+    return bos::host_forward(p, static_cast<cudaStream_t>(stream_), dev);
 }
 
 extern "C" int attn_device_status(void* stream) {

@@ -22,6 +22,11 @@ struct AttnParams {
 // is current). Returns an attn_status code.
 int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev);
 
+// attn_fwd_host's body: `p` holds HOST pointers (validated); stages them through
+// device memory, overlapping copies and compute over chunks of heads, and
+// synchronises `stream` before returning. Returns an attn_status code.
+int host_forward(const AttnParams& p, cudaStream_t stream, int dev);
+
 // Wall-time limit of every wait inside the kernel (0 restores the default).
 void set_wait_limit_ns(uint64_t ns);
 

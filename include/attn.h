@@ -80,10 +80,14 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   lse_h         : fp32 host array [B, H, N], written.
  *   other arguments as for attn_fwd.
  *
- * Copies the inputs to stream-ordered device memory (cudaMallocAsync on
- * `stream`), runs attn_fwd, copies O and LSE back, frees the staging memory
- * and synchronises `stream` before returning, so the host arrays are ready
- * when it returns ATTN_OK. Host pointers need no particular alignment.
+ * Stages the arrays through device memory taken from a library-owned,
+ * stream-ordered memory pool (the pool keeps its memory between calls, up to
+ * the largest problem seen, until the process exits). Large problems are cut
+ * into chunks of whole heads whose host-to-device copies, kernels and
+ * device-to-host copies overlap on internal streams ordered after `stream`.
+ * Synchronises `stream` before returning, so the host arrays are ready when it
+ * returns ATTN_OK. Calls for the same device are serialised internally. Host
+ * pointers need no particular alignment.
  */
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   int B, int H, int N, int d, float scale, int causal, void* stream);
@@ -92,8 +96,8 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
  * attn_fwd_host_noalloc - attn_fwd_host for callers that cannot allocate.
  *
  * The pages have no counterpart to this call. attn_fwd_host stages the host
- * arrays through device memory it allocates on every call; some callers cannot
- * allocate at that point (another framework's caching allocator owns the
+ * arrays through device memory it allocates (from a memory pool) on every
+ * call; some callers cannot allocate at that point (another framework's caching allocator owns the
  * device memory, or the thread must not take the implicit synchronisation an
  * allocation can bring). This entry point computes the same result with no
  * cudaMalloc, cudaMallocAsync or cudaFree: Q, K, V, O and LSE are staged

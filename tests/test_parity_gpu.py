@@ -118,6 +118,23 @@ def test_host_buffer_entry():
     assert_parity(o.float().numpy(), lse.numpy(), o_ref, lse_ref, "host entry")
 
 
+def test_host_buffer_entry_chunked_matches_device_entry():
+    """Large enough that attn_fwd_host pipelines several chunks of heads over its streams."""
+    B, H, N, d = 2, 16, 2048, 128           # 50 MB of inputs -> 3 chunks
+    q, k, v = make_qkv(B, H, N, d, seed=13)
+    scale = float(np.float32(d ** -0.5))
+    o_h = torch.empty_like(q).pin_memory()
+    l_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    bos.attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), o_h, l_h, B, H, N, d, scale, 1)
+    o_d, l_d = run_guarded(q, k, v, scale, True)
+    np.testing.assert_array_equal(o_h.float().numpy(), o_d)
+    np.testing.assert_array_equal(l_h.numpy(), l_d)
+    rows = sample_rows(B, H, N, n_random=16, seed=13)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, True, rows=rows)
+    assert_parity(o_h.float().numpy().reshape(-1, d)[rows], l_h.numpy().reshape(-1)[rows], o_ref, lse_ref,
+                  "host entry, chunked")
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled
 
 @pytest.mark.parametrize("w", [MEDIUM, CAUSAL_2K, CAUSAL_8K, TAIL_4000], ids=lambda w: w.name)
