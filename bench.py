@@ -58,6 +58,21 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's value (the job's time is set by its last replica)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload (weak scaling)."""
+    return flops_per_step * steps * world / seconds / 1e12
+
+
 def kernel_source_hash() -> str:
     """Hash of the attention kernel's sources (the counters in profiles/ are tied to it)."""
     h = hashlib.sha256()
@@ -317,11 +332,8 @@ def run_ours(args, w):
     clocks = sampler.stop()
     total_ms = t_begin.elapsed_time(t_end)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = w.flops * args.steps * world / (total_ms / 1e3) / 1e12
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    value = job_throughput(w.flops, args.steps, world, total_ms / 1e3)
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e_value, e2e_steps = None, 0
@@ -337,11 +349,8 @@ def run_ours(args, w):
         for _ in range(e2e_steps):
             bos.attn_fwd_host(qp, kp, vp, op, lp, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
         e2e_s = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e_value = w.flops * e2e_steps * world / e2e_s / 1e12
+        e2e_s = max_over_ranks(e2e_s, dist, dev)
+        e2e_value = job_throughput(w.flops, e2e_steps, world, e2e_s)
 
     peaks, peaks_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
