@@ -75,24 +75,35 @@ constexpr uint32_t kTmemO = 128;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;         // 1 s
 
+// Barriers (mbarriers in shared memory), by index.
+enum : int {
+    kBarQFull = 0,      // the unit's two Q tiles have landed (TMA transaction count)
+    kBarQEmpty = 1,     // both streams' last S of the unit is complete (two MMA commits)
+    kBarSFull = 2,      // [2] S_t complete (MMA commit)
+    kBarPHalf = 4,      // [2] keys 0-63 of P_t are in tensor memory (128 arrivals)
+    kBarPFull = 6,      // [2] keys 64-127 of P_t are in shared memory (128 arrivals)
+    kBarPbDone = 8,     // [2] PV_t for keys 64-127 complete: O_t current, P_t's shared half free (MMA commit)
+    kBarOStaged = 10,   // [2] a 64-column slice of O_t is in shared memory (128 arrivals)
+    kBarORead = 12,     // [2] the TMA store has read that slice (1 arrival)
+    kBarDrain = 14,     // [2] every MMA of stream t complete (final commit)
+    kBarNever = 16,     // never signalled (test hook)
+    kBarKV = 17,        // kv_full[kStages], then kv_empty[kStages]
+};
+
 template <int D>
 struct Cfg {
     static constexpr int kTileBytes = kBN * D * 2;          // one bf16 Q, K or V tile
-    // K/V ring depth. Three stages keep stream 0 at most about half a block ahead
-    // of stream 1 (measured faster than four on the causal workloads), and with
-    // three stages K_{i+2} reuses V_i's stage, which keeps stream 1's wait for
-    // S_0(i) free of phase aliasing (see mma_issuer).
-    static constexpr int kStages = 3;
+    static constexpr int kPbBytes = kBM * 64 * 2;           // keys 64-127 of P_t (bf16), one 128-byte row per query
+    // K/V ring depth. V_i's stage stays busy until the PV of keys 64-127, which a
+    // stream issues after S(i+1); with four 32 KB stages (d = 128) every load has
+    // about a block of lead.
+    static constexpr int kStages = D == 128 ? 4 : 8;
     static constexpr int kBoxes = D / 64;                   // 64-column TMA boxes per tile
-    // Q is double-buffered (2 buffers x 2 tiles): the next unit's Q tiles load
-    // while the current unit runs, so a unit starts as soon as its K_0 lands.
-    static constexpr int kOffKV = 4 * kTileBytes;
+    // shared memory: Q tiles [2] | second halves of P [2] | K/V ring | barriers | misc
+    static constexpr int kOffPb = 2 * kTileBytes;
+    static constexpr int kOffKV = kOffPb + 2 * kPbBytes;
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-    // barriers: q_full[2], q_empty[2] (per Q buffer), kv_full[S], kv_empty[S], then per Q tile s_full[2], p_half[2],
-    // p_full[2], o_full[2], drain[2], then never (test hook), then s0_done[2] (S_0(i) complete,
-    // slot i & 1, for stream 1), then o_staged[2] (a warpgroup's O tile is in shared memory)
-    static constexpr int kBarTile = 4 + 2 * kStages;
-    static constexpr int kNumBars = kBarTile + 10 + 1 + 2 + 2;
+    static constexpr int kNumBars = kBarKV + 2 * kStages;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slots [2], abort flag
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 };
@@ -186,16 +197,14 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
                          uint8_t* sQ, uint8_t* sKV, uint64_t* bars, volatile int* abort_flag,
                          const KernelArgs& a) {
     using C = Cfg<D>;
-    uint64_t* q_full = bars + 0;      // [2]
-    uint64_t* q_empty = bars + 2;     // [2]
-    uint64_t* kv_full = bars + 4;
-    uint64_t* kv_empty = bars + 4 + C::kStages;
+    uint64_t* kv_full = bars + kBarKV;
+    uint64_t* kv_empty = bars + kBarKV + C::kStages;
     const int total = a.BH * a.U;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0;             // stages with a load whose completion is not yet observed
     uint32_t issued_parity = 0;           // parity of that load's phase, per stage
-    int q_parity[2] = {-1, -1};           // per Q buffer: parity of its last load's phase, -1 before any
+    int q_parity = -1;                    // parity of the last Q load's phase, -1 before any
     bool ok = true;
     // One K/V tile into the next ring stage.
     auto load_kv = [&](const CUtensorMap* tm, int j, int bh) -> bool {
@@ -208,21 +217,19 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         return true;
     };
-    int it = 0;
-    for (int r = 0; ok; ++r, ++it) {
+    for (int r = 0; ok; ++r) {
         const int k = unit_index(r);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
-        // Q tiles first (their buffer was released by the unit before last), then
-        // the unit's K/V stream.
-        const int qb = it & 1;
-        if (!wait_or_abort(&q_empty[qb], ((it >> 1) & 1) ^ 1, a.wait_limit_ns, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&q_full[qb], 2 * C::kTileBytes);
-        q_parity[qb] = (it >> 1) & 1;
+        // Q tiles first, once both streams' last S of the previous unit is done
+        // with the buffer, then the unit's K/V stream.
+        if (!wait_or_abort(&bars[kBarQEmpty], (r & 1) ^ 1, a.wait_limit_ns, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * C::kTileBytes);
+        q_parity = r & 1;
         for (int t = 0; t < 2; ++t)
             for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_3d(sQ + (qb * 2 + t) * C::kTileBytes + b * 16384, tm_q, &q_full[qb], b * 64,
-                            u.row0 + t * kBM, u.bh);
+                tma_load_3d(sQ + t * C::kTileBytes + b * 16384, tm_q, &bars[kBarQFull], b * 64, u.row0 + t * kBM,
+                            u.bh);
         for (int i = 0; i < u.n && ok; ++i) {
             const int j = u.n - 1 - i;
             if (!load_kv(tm_k, j, u.bh) || !load_kv(tm_v, j, u.bh)) { ok = false; break; }
@@ -232,8 +239,7 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     // normal path they already have).
     for (int s = 0; s < C::kStages; ++s)
         if (issued_mask & (1u << s)) mbar_wait(&kv_full[s], (issued_parity >> s) & 1u, kDrainLimitNs);
-    for (int qb = 0; qb < 2; ++qb)
-        if (q_parity[qb] >= 0) mbar_wait(&q_full[qb], (uint32_t)q_parity[qb], kDrainLimitNs);
+    if (q_parity >= 0) mbar_wait(&bars[kBarQFull], (uint32_t)q_parity, kDrainLimitNs);
 }
 
 // S_t = Q_t K^T into the tile's TMEM allocation `tm`.
@@ -249,108 +255,111 @@ __device__ __forceinline__ void issue_s(uint32_t tm, const uint8_t* sQt, const u
     }
 }
 
-// O_t (+)= P_t[:, keys of steps kk0..kk1) * V[those keys, :], in the tile's allocation `tm`.
+// O_t (+)= P_t[:, keys 0-63] * V[keys 0-63, :], P from tensor memory (packed
+// bf16 pairs over the first 32 columns of S_t).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tm, const uint8_t* sV, bool accumulate, int kk0, int kk1) {
+__device__ __forceinline__ void issue_pv_lo(uint32_t tm, const uint8_t* sV, bool accumulate) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
     const uint32_t va = smem_u32(sV);
 #pragma unroll
-    for (int kk = kk0; kk < kk1; ++kk)   // 16 keys per step: 8 P columns, 16 V rows (2048 bytes)
+    for (int kk = 0; kk < 4; ++kk)       // 16 keys per step: 8 P columns, 16 V rows (2048 bytes)
         mma_ts(tm + kTmemO, tm + kTmemS + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), idesc,
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
-
+// O_t += P_t[:, keys 64-127] * V[keys 64-127, :], P from shared memory
+// (K-major, 128-byte swizzle, one 128-byte row per query).
+template <int D>
+__device__ __forceinline__ void issue_pv_hi(uint32_t tm, const uint8_t* sPbt, const uint8_t* sV) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
+    const uint32_t pa = smem_u32(sPbt), va = smem_u32(sV);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tm + kTmemO, sdesc_sw128(pa + kk * 32, 16, 1024), sdesc_sw128(va + (kk + 4) * 2048, 16384, 1024),
+               idesc, 1u);
+}
 
 // One MMA stream: Q tile t's S_t = Q_t K^T and O_t += P_t V, issued by one
-// thread, in the order S(i), PV(i), S(i+1), ... (S(i+1) overwrites P(i), which
-// in-order execution within the stream makes safe). Both streams walk the same
-// K/V ring; a stage is free once both have committed it.
-//
-// The streams are kept half a block apart: stream 1 issues S_1(i) only once
-// S_0(i) has completed, so S_1(i) runs while softmax 0 works on S_0(i), PV_0(i)
-// runs while softmax 1 works on S_1(i), and the two softmax warpgroups rarely
-// compete for the exp2 unit. Stream 0 signals "S_0(i) complete" on barrier
-// s0_done[i & 1]. Stream 1's wait for that signal cannot alias the next one on
-// the same barrier (S_0(i+2)): S_0(i+2) needs K_{i+2}, whose stage (with three
-// stages) is V_i's, freed only after PV_1(i) completes, and stream 1 issues
-// PV_1(i) only after this wait. Nothing in stream 0 waits on stream 1 other than
-// through the ring and the Q buffer, so the order cannot deadlock.
+// thread into the tile's own TMEM allocation, in the order
+//     S(i), PV_lo(i), S(i+1), PV_hi(i), PV_lo(i+1), S(i+2), ...
+// PV_lo(i) reads keys 0-63 of P(i) from the first 32 columns of S_t, so S(i+1)
+// may only overwrite S_t after it, and in-order execution within the stream
+// guarantees that. Keys 64-127 of P(i) live in shared memory, so S(i+1) does
+// not wait for the softmax to finish block i: the tensor core computes the next
+// scores while the softmax is still writing the second half of P.
+// Both streams walk the same K/V ring (K_j, V_j alternating); a stage is free
+// once both have committed it.
 template <int D>
-__device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sKV, uint64_t* bars,
-                           volatile int* abort_flag, const KernelArgs& a) {
+__device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sPb, const uint8_t* sKV,
+                           uint64_t* bars, volatile int* abort_flag, const KernelArgs& a) {
     using C = Cfg<D>;
-    uint64_t* q_full = bars + 0;      // [2]
-    uint64_t* q_empty = bars + 2;     // [2]
-    uint64_t* kv_full = bars + 4;
-    uint64_t* kv_empty = bars + 4 + C::kStages;
-    uint64_t* s_full = bars + C::kBarTile;
-    uint64_t* p_half = s_full + 2;
-    uint64_t* p_full = s_full + 4;
-    uint64_t* o_full = s_full + 6;
-    uint64_t* drain = s_full + 8;      // drain[2]
-    uint64_t* never = s_full + 10;
-    uint64_t* s0_done = s_full + 11;   // [2]
+    uint64_t* kv_full = bars + kBarKV;
+    uint64_t* kv_empty = bars + kBarKV + C::kStages;
+    uint64_t* s_full = bars + kBarSFull + t;
+    uint64_t* p_half = bars + kBarPHalf + t;
+    uint64_t* p_full = bars + kBarPFull + t;
+    uint64_t* pb_done = bars + kBarPbDone + t;
     const uint64_t lim = a.wait_limit_ns;
     const int total = a.BH * a.U;
+    const uint8_t* sQt = sQ + t * C::kTileBytes;
+    const uint8_t* sPbt = sPb + t * C::kPbBytes;
     int stage = 0;
-    uint32_t phase = 0, p_phase = 0;
-    uint32_t s0_count = 0;             // S_0 blocks signalled (stream 0) or awaited (stream 1) so far
+    uint32_t phase = 0, ph_phase = 0, pf_phase = 0;
     bool ok = true;
-    if (t == 0 && a.test_stall && !wait_or_abort(never, 0, lim, abort_flag)) ok = false;
-    int it = 0;
-    for (int r = 0; ok; ++r, ++it) {
+    if (t == 0 && a.test_stall && !wait_or_abort(bars + kBarNever, 0, lim, abort_flag)) ok = false;
+    // the next ring stage in load order, once its tile has landed
+    auto next_stage = [&](int& st) -> bool {
+        st = stage;
+        if (!wait_or_abort(&kv_full[stage], phase, lim, abort_flag)) return false;
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        return true;
+    };
+    // PV_hi of block `i` (if Q tile t takes part in it), then release V_i's stage
+    auto finish_block = [&](int i, int first, int vst) -> bool {
+        if (i >= first) {
+            if (!wait_or_abort(p_full, pf_phase, lim, abort_flag)) return false;
+            pf_phase ^= 1;
+            tc_fence_after();
+            issue_pv_hi<D>(tm, sPbt, sKV + vst * C::kTileBytes);
+            mma_commit(pb_done);
+        }
+        mma_commit(&kv_empty[vst]);
+        return true;
+    };
+    for (int r = 0; ok; ++r) {
         const int k = unit_index(r);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
-        const int first = (t == 0) ? u.first0 : 0;
-        const int qb = it & 1;
-        const uint8_t* sQt = sQ + (qb * 2 + t) * C::kTileBytes;
-        if (!wait_or_abort(&q_full[qb], (it >> 1) & 1, lim, abort_flag)) { ok = false; break; }
+        const int first = (t == 0) ? u.first0 : 0;   // Q tile 0 skips the block past its diagonal
+        if (!wait_or_abort(&bars[kBarQFull], r & 1, lim, abort_flag)) { ok = false; break; }
+        int vprev = -1;                                // V stage of block i-1
         for (int i = 0; i < u.n; ++i) {
             const bool active = (i >= first);
-            const int kst = stage;
-            if (!wait_or_abort(&kv_full[stage], phase, lim, abort_flag)) { ok = false; break; }
-            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-            if (t == 1 && i >= u.first0) {          // tile 0 is active in this block
-                if (!wait_or_abort(&s0_done[s0_count & 1], (s0_count >> 1) & 1, lim, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                ++s0_count;
-            }
+            int kst, vst;
+            if (!next_stage(kst)) { ok = false; break; }
             if (active) {
                 tc_fence_after();
                 issue_s<D>(tm, sQt, sKV + kst * C::kTileBytes);
-                mma_commit(&s_full[t]);
-                if (t == 0) {
-                    mma_commit(&s0_done[s0_count & 1]);
-                    ++s0_count;
-                }
+                mma_commit(s_full);
             }
             mma_commit(&kv_empty[kst]);
-            if (i == u.n - 1) mma_commit(&q_empty[qb]);
-            const int vst = stage;
-            if (!wait_or_abort(&kv_full[stage], phase, lim, abort_flag)) { ok = false; break; }
-            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            if (i == u.n - 1) mma_commit(&bars[kBarQEmpty]);
+            if (vprev >= 0 && !finish_block(i - 1, first, vprev)) { ok = false; break; }
+            if (!next_stage(vst)) { ok = false; break; }
             if (active) {
-                const uint8_t* sV = sKV + vst * C::kTileBytes;
-                // each 64-key half of P_t as soon as the softmax has written it
-                if (!wait_or_abort(&p_half[t], p_phase, lim, abort_flag)) { ok = false; break; }
+                if (!wait_or_abort(p_half, ph_phase, lim, abort_flag)) { ok = false; break; }
+                ph_phase ^= 1;
                 tc_fence_after();
-                issue_pv<D>(tm, sV, i > first, 0, kBN / 32);
-                if (!wait_or_abort(&p_full[t], p_phase, lim, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                issue_pv<D>(tm, sV, true, kBN / 32, kBN / 16);
-                p_phase ^= 1;
-                if (i == u.n - 1) mma_commit(&o_full[t]);
+                issue_pv_lo<D>(tm, sKV + vst * C::kTileBytes, i > first);
             }
-            mma_commit(&kv_empty[vst]);
+            vprev = vst;
         }
+        if (!ok) break;
+        if (!finish_block(u.n - 1, first, vprev)) { ok = false; break; }
     }
     // Every MMA this thread issued must complete before tensor memory is freed.
-    mma_commit(&drain[t]);
-    mbar_wait(&drain[t], 0, kDrainLimitNs);
+    mma_commit(&bars[kBarDrain + t]);
+    mbar_wait(&bars[kBarDrain + t], 0, kDrainLimitNs);
 }
 
 // Packed fp32 pair helpers (sm_100 family: one instruction for two lanes of work).
@@ -435,12 +444,12 @@ __device__ __forceinline__ float masked_row_max(const uint32_t (&sr)[128], float
 }
 
 // exp2 of 32 scores (keys 32*ch .. 32*ch+31): x = s * c - m in one packed FMA per
-// pair, p = 2^x (0 for columns >= lim when kMasked), written to P_t as 16 packed
-// bf16 pairs; the fp32 probabilities are added pairwise into acc[4].
+// pair, p = 2^x (0 for columns >= lim when kMasked), packed into 16 bf16 pairs
+// (key 2e in the low half of pk[e]); the fp32 probabilities are added pairwise
+// into acc[4].
 template <bool kMasked>
-__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[128], int ch, uint64_t c2, uint64_t negm2,
-                                          uint64_t (&acc)[4], uint32_t tS, int lim) {
-    uint32_t pk[16];
+__device__ __forceinline__ void exp_pack(const uint32_t (&sr)[128], int ch, uint64_t c2, uint64_t negm2,
+                                         uint64_t (&acc)[4], int lim, uint32_t (&pk)[16]) {
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
         const int c0 = ch * 32 + 2 * e;
@@ -455,34 +464,72 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[128], int ch, uin
         acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
         pk[e] = pack_bf16(p0, p1);
     }
-    tmem_st16(tS + ch * 16, pk);
+}
+
+// Keys 0-63 of P_t: chunks 0 and 1 into tensor memory (over S_t's first 32 columns).
+template <bool kMasked>
+__device__ __forceinline__ void p_lo_to_tmem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
+                                             uint64_t (&acc)[4], int lim, uint32_t tS) {
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        uint32_t pk[16];
+        exp_pack<kMasked>(sr, ch, c2, negm2, acc, lim, pk);
+        tmem_st16(tS + ch * 16, pk);
+    }
+}
+
+// Keys 64-127 of P_t: chunks 2 and 3 into this row of the shared-memory half,
+// K-major with the 128-byte swizzle (16-byte chunk q of the row at q ^ (row & 7)).
+template <bool kMasked>
+__device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
+                                             uint64_t (&acc)[4], int lim, uint8_t* prow, int swz) {
+#pragma unroll
+    for (int ch = 2; ch < 4; ++ch) {
+        uint32_t pk[16];
+        exp_pack<kMasked>(sr, ch, c2, negm2, acc, lim, pk);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c16 = (ch - 2) * 4 + q;
+            *reinterpret_cast<uint4*>(prow + ((c16 ^ swz) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+    }
 }
 
 // Softmax warpgroup of Q tile t (thread = query row = TMEM lane). After a unit's
-// last block it also writes the unit's O tile: O / l as bf16 into the unit's own
-// Q_t buffer (free once PV_t of the last block is done) in the 128-byte-swizzled
-// layout, then one thread stores it with TMA (rows past N are clipped) and
-// releases the Q buffer once the store has read it.
+// last block it also writes the unit's O tile: O / l as bf16, one 64-column
+// slice at a time through the tile's shared half of P (free once the last PV
+// is done) in the 128-byte-swizzled layout, stored by one thread with TMA (rows
+// past N are clipped).
 template <int D>
 __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, volatile int* abort_flag,
-                             uint8_t* sQ, const CUtensorMap* tm_o, const KernelArgs& a) {
+                             uint8_t* sPb, const CUtensorMap* tm_o, const KernelArgs& a) {
     using C = Cfg<D>;
-    uint64_t* q_empty = bars + 2;     // [2]
-    uint64_t* s_full = bars + C::kBarTile;
-    uint64_t* p_half = s_full + 2;
-    uint64_t* p_full = s_full + 4;
-    uint64_t* o_full = s_full + 6;
-    uint64_t* o_staged = s_full + 13;  // [2]
+    uint64_t* s_full = bars + kBarSFull + t;
+    uint64_t* p_half = bars + kBarPHalf + t;
+    uint64_t* p_full = bars + kBarPFull + t;
+    uint64_t* pb_done = bars + kBarPbDone + t;
+    uint64_t* o_staged = bars + kBarOStaged + t;
+    uint64_t* o_read = bars + kBarORead + t;
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t lane_base = tm + ((uint32_t)(wq * 32) << 16);
     const uint32_t tS = lane_base + kTmemS;
     const uint32_t tO = lane_base + kTmemO;
     const int row_in_tile = wq * 32 + lane;
+    uint8_t* sPbt = sPb + t * C::kPbBytes;
+    uint8_t* prow = sPbt + row_in_tile * 128;
+    const int swz = row_in_tile & 7;
     const float c = a.scale_log2;
     const uint64_t c2 = f2_pack(c, c);
     const int total = a.BH * a.U;
-    uint32_t s_phase = 0, o_phase = 0;
+    uint32_t s_phase = 0, pb_phase = 0, os_phase = 0, or_phase = 0;
+    bool or_pending = false;   // the last O slice's store may still be reading the shared half of P
     bool ok = true;
+    // bounded wait shared by the whole warp
+    auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+        bool got = wait_or_abort(bar, parity, lim, abort_flag);
+        return __all_sync(0xffffffffu, got);
+    };
     for (int r = 0; ok; ++r) {
         const int k = unit_index(r);
         if (k >= total) break;
@@ -494,9 +541,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         float l = 0.f;
         for (int i = first; i < u.n; ++i) {
             const int j = u.n - 1 - i;
-            bool got = wait_or_abort(&s_full[t], s_phase, lim, abort_flag);
-            got = __all_sync(0xffffffffu, got);
-            if (!got) { ok = false; break; }
+            if (!wait_warp(s_full, s_phase)) { ok = false; break; }
             s_phase ^= 1;
             tc_fence_after();
             uint32_t sr[128];
@@ -514,9 +559,11 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 tmem_ld128(tS, sr);
                 m_tile = (c >= 0.f) ? row_extreme<true>(sr) * c : row_extreme<false>(sr) * c;
             }
+            // PV_hi of the previous block must be complete before O_t is rescaled
+            // or the shared half of P_t is rewritten.
+            bool pb_pending = (i > first);
             // Move the reference max only when the block's max exceeds it by more
-            // than 2^8; then rescale O_t (complete up to the previous block: the
-            // commit behind s_full covers every earlier MMA) and l.
+            // than 2^8; then rescale O_t and l.
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 m_ref = m_tile;
@@ -525,6 +572,12 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 m_ref = m_tile;
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (pb_pending) {
+                    if (!wait_warp(pb_done, pb_phase)) { ok = false; break; }
+                    pb_phase ^= 1;
+                    pb_pending = false;
+                    tc_fence_after();
+                }
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t orow[32];
@@ -537,27 +590,26 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint64_t negm2 = f2_pack(negm, negm);
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
-            // first 64 keys: hand P's first half to the MMA as soon as it is in TMEM
-            if (need_mask) {
-                exp_chunk<true>(sr, 0, c2, negm2, acc, tS, lim);
-                exp_chunk<true>(sr, 1, c2, negm2, acc, tS, lim);
-            } else {
-                exp_chunk<false>(sr, 0, c2, negm2, acc, tS, lim);
-                exp_chunk<false>(sr, 1, c2, negm2, acc, tS, lim);
-            }
+            // keys 0-63 into tensor memory; the MMA takes them (and then computes the
+            // next block's scores) while keys 64-127 are being exponentiated
+            if (need_mask) p_lo_to_tmem<true>(sr, c2, negm2, acc, lim, tS);
+            else p_lo_to_tmem<false>(sr, c2, negm2, acc, lim, tS);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_half[t]);
-            if (need_mask) {
-                exp_chunk<true>(sr, 2, c2, negm2, acc, tS, lim);
-                exp_chunk<true>(sr, 3, c2, negm2, acc, tS, lim);
-            } else {
-                exp_chunk<false>(sr, 2, c2, negm2, acc, tS, lim);
-                exp_chunk<false>(sr, 3, c2, negm2, acc, tS, lim);
+            mbar_arrive(p_half);
+            if (pb_pending) {
+                if (!wait_warp(pb_done, pb_phase)) { ok = false; break; }
+                pb_phase ^= 1;
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&p_full[t]);
+            if (or_pending) {
+                if (!wait_warp(o_read, or_phase)) { ok = false; break; }
+                or_phase ^= 1;
+                or_pending = false;
+            }
+            if (need_mask) p_hi_to_smem<true>(sr, c2, negm2, acc, lim, prow, swz);
+            else p_hi_to_smem<false>(sr, c2, negm2, acc, lim, prow, swz);
+            fence_proxy_async_smem();
+            mbar_arrive(p_full);
             const uint64_t s01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
             float sum0, sum1;
             f2_unpack(s01, sum0, sum1);
@@ -565,10 +617,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         }
         if (!ok) break;
         // epilogue: O / l -> bf16 through shared memory and TMA, LSE in natural log
-        bool got = wait_or_abort(&o_full[t], o_phase, lim, abort_flag);
-        got = __all_sync(0xffffffffu, got);
-        if (!got) { ok = false; break; }
-        o_phase ^= 1;
+        if (!wait_warp(pb_done, pb_phase)) { ok = false; break; }   // the unit's last PV is complete
+        pb_phase ^= 1;
         tc_fence_after();
         const float l_safe = (l > 0.f) ? l : 1.f;
         const float inv = 1.f / l_safe;
@@ -581,35 +631,39 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             tmem_ld32(tO, h0);
             tmem_ld32(tO + 32, h1);
         }
-        const int qb = r & 1;
-        uint8_t* stage = sQ + (qb * 2 + t) * C::kTileBytes;
-        uint8_t* srow = stage + row_in_tile * 128;
-        const int swz = row_in_tile & 7;
-#pragma unroll
-        for (int c16 = 0; c16 < D / 8; ++c16) {     // 16-byte chunk = 8 output columns
-            const int col = c16 * 8;
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
-            // 64-column box (c16 / 8), 128-byte swizzle: chunk index XOR (row & 7)
-            *reinterpret_cast<uint4*>(srow + (c16 >> 3) * 16384 + (((c16 & 7) ^ swz) << 4)) = w;
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&o_staged[t]);
-        if (row_in_tile == 0) {
-            // a bounded wait, so a warp that aborted cannot leave this thread stuck
-            if (wait_or_abort(&o_staged[t], o_phase ^ 1, lim, abort_flag)) {
-                for (int b = 0; b < C::kBoxes; ++b)
-                    tma_store_3d(tm_o, stage + b * 16384, b * 64, tile_row0, u.bh);
-                bulk_commit();
-                bulk_wait_read0();
-                mbar_arrive(&q_empty[qb]);
-            }
-        }
-        if (row < a.N) a.lse[(int64_t)u.bh * a.N + row] = (m_ref + log2f(l_safe)) * 0.69314718055994531f;
         tc_fence_before();
+#pragma unroll
+        for (int s = 0; s < C::kBoxes; ++s) {
+            if (s > 0) {   // the previous slice's store has read the buffer
+                if (!wait_warp(o_read, or_phase)) { ok = false; break; }
+                or_phase ^= 1;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {     // 16-byte chunk = 8 output columns
+                const int col = s * 64 + q * 8;
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
+                w.y = pack_bf16(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
+                w.z = pack_bf16(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
+                w.w = pack_bf16(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
+                *reinterpret_cast<uint4*>(prow + ((q ^ swz) << 4)) = w;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(o_staged);
+            if (row_in_tile == 0) {
+                // a bounded wait, so a warp that aborted cannot leave this thread stuck
+                if (wait_or_abort(o_staged, os_phase, lim, abort_flag)) {
+                    tma_store_3d(tm_o, sPbt, s * 64, tile_row0, u.bh);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(o_read);
+                }
+            }
+            os_phase ^= 1;
+        }
+        if (!ok) break;
+        or_pending = true;
+        if (row < a.N) a.lse[(int64_t)u.bh * a.N + row] = (m_ref + log2f(l_safe)) * 0.69314718055994531f;
     }
     if (row_in_tile == 0) bulk_wait0();   // this warpgroup's O stores are complete
 }
@@ -625,6 +679,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem;
+    uint8_t* sPb = smem + C::kOffPb;
     uint8_t* sKV = smem + C::kOffKV;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [2]
@@ -632,29 +687,22 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        for (int qb = 0; qb < 2; ++qb) {
-            mbar_init(bars + qb, 1);                             // q_full[qb]
-            mbar_init(bars + 2 + qb, 4);                         // q_empty[qb]: a commit per MMA stream, an
-                                                                 // arrival per softmax warpgroup (O stored)
-        }
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bars + 4 + s, 1);                          // kv_full
-            mbar_init(bars + 4 + C::kStages + s, 2);             // kv_empty: one commit per MMA stream
-        }
-        uint64_t* s_full = bars + C::kBarTile;
+        mbar_init(&bars[kBarQFull], 1);
+        mbar_init(&bars[kBarQEmpty], 2);                         // one commit per MMA stream
         for (int t = 0; t < 2; ++t) {
-            mbar_init(s_full + t, 1);                            // s_full: MMA commit
-            mbar_init(s_full + 2 + t, kBM);                      // p_half: every softmax thread arrives
-            mbar_init(s_full + 4 + t, kBM);                      // p_full: every softmax thread arrives
-            mbar_init(s_full + 6 + t, 1);                        // o_full: MMA commit
+            mbar_init(&bars[kBarSFull + t], 1);                  // MMA commit
+            mbar_init(&bars[kBarPHalf + t], kBM);                // every softmax thread arrives
+            mbar_init(&bars[kBarPFull + t], kBM);
+            mbar_init(&bars[kBarPbDone + t], 1);                 // MMA commit
+            mbar_init(&bars[kBarOStaged + t], kBM);              // every softmax thread arrives
+            mbar_init(&bars[kBarORead + t], 1);                  // the storing thread arrives
+            mbar_init(&bars[kBarDrain + t], 1);
         }
-        mbar_init(s_full + 8, 1);                                // drain, stream 0
-        mbar_init(s_full + 9, 1);                                // drain, stream 1
-        mbar_init(s_full + 10, 1);                               // never (test hook)
-        mbar_init(s_full + 11, 1);                               // s0_done[0]
-        mbar_init(s_full + 12, 1);                               // s0_done[1]
-        mbar_init(s_full + 13, kBM);                             // o_staged[0]: every softmax thread arrives
-        mbar_init(s_full + 14, kBM);                             // o_staged[1]
+        mbar_init(&bars[kBarNever], 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars[kBarKV + s], 1);                     // kv_full
+            mbar_init(&bars[kBarKV + C::kStages + s], 2);        // kv_empty: one commit per MMA stream
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -676,7 +724,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
     if (warp < kWarpProducer) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, abort_flag, sQ, &tm_o, a);
+        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, abort_flag, sPb, &tm_o, a);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
@@ -684,7 +732,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             __syncwarp();
         } else if (warp == kWarpMma0 || warp == kWarpMma1) {
             const int t = warp - kWarpMma0;
-            if (lane == 0) mma_issuer<D>(t ? tmem1 : tmem0, t, sQ, sKV, bars, abort_flag, a);
+            if (lane == 0) mma_issuer<D>(t ? tmem1 : tmem0, t, sQ, sPb, sKV, bars, abort_flag, a);
             __syncwarp();
         }
     }
@@ -697,7 +745,6 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tmem_dealloc(tmem1, kTmemColsPerTile);
     }
 }
-
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
