@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -83,12 +84,14 @@ enum : int {
     kBarPHalf = 4,      // [2] keys 0-63 of P_t are in tensor memory (128 arrivals)
     kBarPFull = 6,      // [2] keys 64-127 of P_t are in shared memory (128 arrivals)
     kBarPbDone = 8,     // [2] PV_t for keys 64-127 complete: O_t current, P_t's shared half free (MMA commit)
-    kBarOStaged = 10,   // [2] a 64-column slice of O_t is in shared memory (128 arrivals)
-    kBarORead = 12,     // [2] the TMA store has read that slice (1 arrival)
-    kBarDrain = 14,     // [2] every MMA of stream t complete (final commit)
-    kBarNever = 16,     // never signalled (test hook)
-    kBarKV = 17,        // kv_full[kStages], then kv_empty[kStages]
+    kBarDrain = 10,     // [2] every MMA of stream t complete (final commit)
+    kBarNever = 12,     // never signalled (test hook)
+    kBarUnitFull = 13,  // [kUnitRing] the producer has written the next unit index (1 arrival)
+    kBarUnitEmpty = 17, // [kUnitRing] every role has read it (2 MMA threads + 8 softmax warps)
+    kBarKV = 21,        // kv_full[kStages], then kv_empty[kStages]
 };
+constexpr int kUnitRing = 4;              // unit indices handed from the producer to the other roles
+constexpr int kUnitReaders = 2 + 8;
 
 template <int D>
 struct Cfg {
@@ -104,8 +107,8 @@ struct Cfg {
     static constexpr int kOffKV = kOffPb + 2 * kPbBytes;
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
     static constexpr int kNumBars = kBarKV + 2 * kStages;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slots [2], abort flag
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slots [2], abort flag, unit ring [4]
+    static constexpr int kSmemBytes = kOffMisc + 32 + 1024;  // + alignment slack
 };
 
 struct KernelArgs {
@@ -115,12 +118,19 @@ struct KernelArgs {
     float* lse;
     uint64_t wait_limit_ns;
     int test_stall;   // test hook: the MMA thread first waits on a barrier nothing signals
+    unsigned int* sched;   // this launch's work counter and exit counter (both zero at launch)
 };
 
 }  // namespace
 
 // Sticky device-side status: 0, or the attn_status of the first failure.
 __device__ int g_attn_device_status;
+
+// Work counters, two words per slot: units taken, CTAs finished. Each launch
+// draws the next slot round-robin and its last CTA zeroes the slot again, so a
+// slot is only reused thousands of launches later, long after its kernel ended.
+constexpr int kSchedSlots = 4096;
+__device__ unsigned int g_attn_sched[2 * kSchedSlots];
 
 namespace {
 
@@ -173,11 +183,22 @@ __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
     return u;
 }
 
-// k-th unit of this CTA: snake order over the grid.
-__device__ __forceinline__ int unit_index(int r) {
-    const int G = gridDim.x, g = blockIdx.x;
-    return r * G + ((r & 1) ? (G - 1 - g) : g);
-}
+// The unit ring: the producer takes each unit index from the launch's global
+// counter (units are numbered heaviest first, so CTAs that run faster simply
+// take more of them) and hands it to the MMA and softmax roles in order.
+// Index >= total means no work is left.
+struct UnitRing {
+    uint64_t* bars;
+    volatile int* idx;   // [kUnitRing]
+    // reader side: the r-th unit index of this CTA, or false if a wait failed
+    __device__ __forceinline__ bool get(int r, int& k, uint64_t lim, volatile int* abort_flag) const {
+        const int sl = r % kUnitRing;
+        if (!wait_or_abort(&bars[kBarUnitFull + sl], (uint32_t)((r / kUnitRing) & 1), lim, abort_flag)) return false;
+        k = idx[sl];
+        return true;
+    }
+    __device__ __forceinline__ void release(int r) const { mbar_arrive(&bars[kBarUnitEmpty + r % kUnitRing]); }
+};
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -194,7 +215,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                         uint8_t* sQ, uint8_t* sKV, uint64_t* bars, volatile int* abort_flag,
+                         uint8_t* sQ, uint8_t* sKV, uint64_t* bars, const UnitRing& ring, volatile int* abort_flag,
                          const KernelArgs& a) {
     using C = Cfg<D>;
     uint64_t* kv_full = bars + kBarKV;
@@ -218,7 +239,15 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         return true;
     };
     for (int r = 0; ok; ++r) {
-        const int k = unit_index(r);
+        const int sl = r % kUnitRing;
+        if (!wait_or_abort(&bars[kBarUnitEmpty + sl], (uint32_t)((r / kUnitRing) & 1) ^ 1, a.wait_limit_ns,
+                           abort_flag)) {
+            ok = false;
+            break;
+        }
+        const int k = (int)atomicAdd(a.sched, 1u);
+        ring.idx[sl] = k;
+        mbar_arrive(&bars[kBarUnitFull + sl]);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
         // Q tiles first, once both streams' last S of the previous unit is done
@@ -291,7 +320,7 @@ __device__ __forceinline__ void issue_pv_hi(uint32_t tm, const uint8_t* sPbt, co
 // once both have committed it.
 template <int D>
 __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sPb, const uint8_t* sKV,
-                           uint64_t* bars, volatile int* abort_flag, const KernelArgs& a) {
+                           uint64_t* bars, const UnitRing& ring, volatile int* abort_flag, const KernelArgs& a) {
     using C = Cfg<D>;
     uint64_t* kv_full = bars + kBarKV;
     uint64_t* kv_empty = bars + kBarKV + C::kStages;
@@ -327,7 +356,9 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
         return true;
     };
     for (int r = 0; ok; ++r) {
-        const int k = unit_index(r);
+        int k;
+        if (!ring.get(r, k, lim, abort_flag)) { ok = false; break; }
+        ring.release(r);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
         const int first = (t == 0) ? u.first0 : 0;   // Q tile 0 skips the block past its diagonal
@@ -499,18 +530,17 @@ __device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t
 // Softmax warpgroup of Q tile t (thread = query row = TMEM lane). After a unit's
 // last block it also writes the unit's O tile: O / l as bf16, one 64-column
 // slice at a time through the tile's shared half of P (free once the last PV
-// is done) in the 128-byte-swizzled layout, stored by one thread with TMA (rows
-// past N are clipped).
+// is done) in the 128-byte-swizzled layout. Each warp stores its own 32 rows
+// with TMA (rows past N are clipped), so the epilogue needs no barrier wider
+// than a warp.
 template <int D>
-__device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, volatile int* abort_flag,
-                             uint8_t* sPb, const CUtensorMap* tm_o, const KernelArgs& a) {
+__device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, const UnitRing& ring,
+                             volatile int* abort_flag, uint8_t* sPb, const CUtensorMap* tm_o, const KernelArgs& a) {
     using C = Cfg<D>;
     uint64_t* s_full = bars + kBarSFull + t;
     uint64_t* p_half = bars + kBarPHalf + t;
     uint64_t* p_full = bars + kBarPFull + t;
     uint64_t* pb_done = bars + kBarPbDone + t;
-    uint64_t* o_staged = bars + kBarOStaged + t;
-    uint64_t* o_read = bars + kBarORead + t;
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t lane_base = tm + ((uint32_t)(wq * 32) << 16);
     const uint32_t tS = lane_base + kTmemS;
@@ -518,12 +548,12 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
     const int row_in_tile = wq * 32 + lane;
     uint8_t* sPbt = sPb + t * C::kPbBytes;
     uint8_t* prow = sPbt + row_in_tile * 128;
+    uint8_t* pwarp = sPbt + wq * 32 * 128;   // this warp's 32 rows (4 KB, 1024-byte aligned)
     const int swz = row_in_tile & 7;
     const float c = a.scale_log2;
     const uint64_t c2 = f2_pack(c, c);
     const int total = a.BH * a.U;
-    uint32_t s_phase = 0, pb_phase = 0, os_phase = 0, or_phase = 0;
-    bool or_pending = false;   // the last O slice's store may still be reading the shared half of P
+    uint32_t s_phase = 0, pb_phase = 0;
     bool ok = true;
     // bounded wait shared by the whole warp
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -531,7 +561,11 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         return __all_sync(0xffffffffu, got);
     };
     for (int r = 0; ok; ++r) {
-        const int k = unit_index(r);
+        int k;
+        bool got = ring.get(r, k, lim, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        __syncwarp();
+        if (lane == 0) ring.release(r);
         if (k >= total) break;
         const Unit u = decode_unit(k, a);
         const int tile_row0 = u.row0 + t * kBM;
@@ -601,11 +635,6 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 if (!wait_warp(pb_done, pb_phase)) { ok = false; break; }
                 pb_phase ^= 1;
             }
-            if (or_pending) {
-                if (!wait_warp(o_read, or_phase)) { ok = false; break; }
-                or_phase ^= 1;
-                or_pending = false;
-            }
             if (need_mask) p_hi_to_smem<true>(sr, c2, negm2, acc, lim, prow, swz);
             else p_hi_to_smem<false>(sr, c2, negm2, acc, lim, prow, swz);
             fence_proxy_async_smem();
@@ -634,10 +663,6 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         tc_fence_before();
 #pragma unroll
         for (int s = 0; s < C::kBoxes; ++s) {
-            if (s > 0) {   // the previous slice's store has read the buffer
-                if (!wait_warp(o_read, or_phase)) { ok = false; break; }
-                or_phase ^= 1;
-            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {     // 16-byte chunk = 8 output columns
                 const int col = s * 64 + q * 8;
@@ -649,23 +674,17 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 *reinterpret_cast<uint4*>(prow + ((q ^ swz) << 4)) = w;
             }
             fence_proxy_async_smem();
-            mbar_arrive(o_staged);
-            if (row_in_tile == 0) {
-                // a bounded wait, so a warp that aborted cannot leave this thread stuck
-                if (wait_or_abort(o_staged, os_phase, lim, abort_flag)) {
-                    tma_store_3d(tm_o, sPbt, s * 64, tile_row0, u.bh);
-                    bulk_commit();
-                    bulk_wait_read0();
-                    mbar_arrive(o_read);
-                }
+            __syncwarp();
+            if (lane == 0) {   // this warp's 32 rows; the buffer is rewritten only after the store has read it
+                tma_store_3d(tm_o, pwarp, s * 64, tile_row0 + wq * 32, u.bh);
+                bulk_commit();
+                bulk_wait_read0();
             }
-            os_phase ^= 1;
+            __syncwarp();
         }
-        if (!ok) break;
-        or_pending = true;
         if (row < a.N) a.lse[(int64_t)u.bh * a.N + row] = (m_ref + log2f(l_safe)) * 0.69314718055994531f;
     }
-    if (row_in_tile == 0) bulk_wait0();   // this warpgroup's O stores are complete
+    if (lane == 0) bulk_wait0();   // this warp's O stores are complete
 }
 
 // ------------------------------------------------------------------ kernel
@@ -684,6 +703,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    const UnitRing ring{bars, reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
@@ -694,11 +714,13 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             mbar_init(&bars[kBarPHalf + t], kBM);                // every softmax thread arrives
             mbar_init(&bars[kBarPFull + t], kBM);
             mbar_init(&bars[kBarPbDone + t], 1);                 // MMA commit
-            mbar_init(&bars[kBarOStaged + t], kBM);              // every softmax thread arrives
-            mbar_init(&bars[kBarORead + t], 1);                  // the storing thread arrives
             mbar_init(&bars[kBarDrain + t], 1);
         }
         mbar_init(&bars[kBarNever], 1);
+        for (int sl = 0; sl < kUnitRing; ++sl) {
+            mbar_init(&bars[kBarUnitFull + sl], 1);
+            mbar_init(&bars[kBarUnitEmpty + sl], kUnitReaders);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars[kBarKV + s], 1);                     // kv_full
             mbar_init(&bars[kBarKV + C::kStages + s], 2);        // kv_empty: one commit per MMA stream
@@ -724,15 +746,15 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
     if (warp < kWarpProducer) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, abort_flag, sPb, &tm_o, a);
+        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, ring, abort_flag, sPb, &tm_o, a);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
-            if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, abort_flag, a);
+            if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, a);
             __syncwarp();
         } else if (warp == kWarpMma0 || warp == kWarpMma1) {
             const int t = warp - kWarpMma0;
-            if (lane == 0) mma_issuer<D>(t ? tmem1 : tmem0, t, sQ, sPb, sKV, bars, abort_flag, a);
+            if (lane == 0) mma_issuer<D>(t ? tmem1 : tmem0, t, sQ, sPb, sKV, bars, ring, abort_flag, a);
             __syncwarp();
         }
     }
@@ -743,6 +765,15 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (warp == kWarpMma0) {
         tmem_dealloc(tmem0, kTmemColsPerTile);
         tmem_dealloc(tmem1, kTmemColsPerTile);
+    }
+    // The last CTA out returns the launch's counters to zero for the next launch
+    // that draws this slot.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(a.sched, 0u);
+            atomicExch(a.sched + 1, 0u);
+        }
     }
 }
 // ------------------------------------------------------------------ host side
@@ -767,12 +798,12 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); 64x128 boxes, 128-byte
-// swizzle; loads read rows past N as zero, stores drop them.
-bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH, int N, int D) {
+// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); boxes of 64 columns x
+// `rows` rows, 128-byte swizzle; loads read rows past N as zero, stores drop them.
+bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH, int N, int D, int rows) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kBN, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -781,6 +812,7 @@ bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH,
 
 uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
 int g_test_stall = 0;
+std::atomic<unsigned int> g_sched_next{0};
 
 template <int D>
 int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
@@ -789,11 +821,13 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     if (!enc) return ATTN_ERR_CUDA;
     const int BH = p.B * p.H;
     CUtensorMap mq, mk, mv, mo;
-    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, D) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, D) ||
-        !encode_qkv_map(enc, &mv, p.v, BH, p.N, D) || !encode_qkv_map(enc, &mo, p.o, BH, p.N, D))
+    // Q, K and V move in 128-row boxes; O is stored 32 rows (one warp) at a time
+    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, D, kBM) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, D, kBN) ||
+        !encode_qkv_map(enc, &mv, p.v, BH, p.N, D, kBN) || !encode_qkv_map(enc, &mo, p.o, BH, p.N, D, 32))
         return ATTN_ERR_BAD_SHAPE;
     static int sms_cache[64] = {0};
     static int attr_done[64] = {0};
+    static unsigned int* sched_cache[64] = {nullptr};
     int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
     if (sms == 0) {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -801,6 +835,16 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
             return ATTN_ERR_CUDA;
         }
         if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+    }
+    unsigned int* sched = (dev >= 0 && dev < 64) ? sched_cache[dev] : nullptr;
+    if (sched == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_attn_sched) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        sched = static_cast<unsigned int*>(ptr);
+        if (dev >= 0 && dev < 64) sched_cache[dev] = sched;
     }
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         if (cudaFuncSetAttribute(attn_fwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -820,6 +864,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.lse = p.lse;
     a.wait_limit_ns = g_wait_limit_ns;
     a.test_stall = g_test_stall;
+    a.sched = sched + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
     const int64_t units = (int64_t)BH * a.U;
     const int grid = (int)(units < sms ? units : sms);
     attn_fwd_sm103_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a);
