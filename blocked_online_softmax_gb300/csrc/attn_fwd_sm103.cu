@@ -11,27 +11,32 @@
 //
 // GB300 design (what differs from the page's Triton kernel):
 //  * Work unit = 256 query rows of one (batch, head) = two 128-row Q tiles that
-//    share every K/V tile. CTAs are persistent (one per SM) and walk a static
-//    list of units: for causal masking the list is heaviest-first over all heads
-//    and dealt to CTAs in snake order, which balances the triangle of work.
+//    share every K/V tile. CTAs are persistent (one per SM) and take units from
+//    a per-launch global counter; units are numbered heaviest first (for causal
+//    masking, over all heads), so the triangle of work balances itself and SMs
+//    that run slower simply take fewer units.
 //  * Warp roles (384 threads): warpgroups 0 and 1 run the softmax of Q tile 0
 //    and Q tile 1, one thread per query row, with 208 registers each after a
-//    setmaxnreg split; warp 8 issues TMA loads (Q per unit, then K_j, V_j into
-//    a multi-stage ring); warp 9 owns the tensor-memory allocation and issues
-//    tcgen05 MMAs from one thread.
-//  * Tensor memory (512 columns x 128 lanes): S_t = Q_t K^T (fp32, 128 cols per
-//    tile), P_t (bf16, written over the first 64 columns of S_t) and O_t (fp32,
-//    d columns). O += P V takes P straight from tensor memory.
-//  * MMA order PV_0(i), S_0(i+1), PV_1(i), S_1(i+1): while one softmax
-//    warpgroup works on its tile, the tensor core runs the other tile's MMAs.
-//  * Key blocks are visited from the last to the first, so the only masked
-//    blocks (the causal diagonal, the ragged tail past N) come first and the
-//    steady-state loop has no masking. Causal: blocks past a tile's diagonal are
-//    skipped, as in the page's loop bound.
+//    setmaxnreg split; warp 8 takes units and issues TMA loads (Q per unit, then
+//    K_j, V_j into a multi-stage ring); warps 9 and 10 each issue the tcgen05
+//    MMAs of one Q tile from one thread (two independent MMA streams keep the
+//    tensor core busy; one stream alone cannot).
+//  * Tensor memory: one 256-column allocation per Q tile holding S_t = Q_t K^T
+//    (fp32, 128 columns) and O_t (fp32, d columns). Keys 0-63 of P_t are written
+//    back as bf16 over S_t's first 32 columns and multiplied from there (TS
+//    MMA); keys 64-127 go to a swizzled shared-memory buffer (SS MMA). Because
+//    only the first half aliases S_t, each stream issues S(i), PV_lo(i), S(i+1),
+//    PV_hi(i): the next scores are computed while the softmax is still
+//    exponentiating the second half of the block.
+//  * Key blocks are visited from the last to the first, so the masked blocks
+//    (the causal diagonal, the ragged tail past N) come first. Causal: blocks
+//    past a tile's diagonal are skipped, as in the page's loop bound.
 //  * The running max is only moved (and O, l rescaled) when a block's max
 //    exceeds it by more than 8 in log2 units; otherwise exponentials are taken
 //    against the older, smaller max (p <= 2^8). O/l and LSE are unchanged in
 //    exact arithmetic, and the O rescale through tensor memory becomes rare.
+//  * Epilogue: O / l as bf16 through the tile's shared P buffer, one TMA store
+//    per warp (32 rows), fp32 LSE with plain stores.
 //  * Every wait is bounded in wall time: on expiry the kernel records a status,
 //    drains its own copies and MMAs, frees tensor memory and returns.
 #include <cuda.h>
