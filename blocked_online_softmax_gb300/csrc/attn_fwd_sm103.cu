@@ -190,7 +190,8 @@ __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
 
 // The unit ring: the producer takes each unit index from the launch's global
 // counter (units are numbered heaviest first, so CTAs that run faster simply
-// take more of them) and hands it to the MMA and softmax roles in order.
+// take more of them; a CTA's first unit is its own index, which saves a global
+// atomic on the start-up path) and hands it to the MMA and softmax roles in order.
 // Index >= total means no work is left.
 struct UnitRing {
     uint64_t* bars;
@@ -250,7 +251,9 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
             ok = false;
             break;
         }
-        const int k = (int)atomicAdd(a.sched, 1u);
+        // the first unit of CTA g is g (the grid never exceeds the unit count); the
+        // counter hands out the rest
+        const int k = (r == 0) ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
         ring.idx[sl] = k;
         mbar_arrive(&bars[kBarUnitFull + sl]);
         if (k >= total) break;
@@ -748,6 +751,12 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem0 = tmem_slot[0], tmem1 = tmem_slot[1];
+    // Launched with programmatic stream serialization: the set-up above may run
+    // while the previous kernel in the stream finishes; nothing in global memory
+    // is read or written before that kernel has completed. A later launch of
+    // this kernel may likewise start its set-up on SMs this grid has left.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kWarpProducer) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -872,8 +881,21 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.sched = sched + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
     const int64_t units = (int64_t)BH * a.U;
     const int grid = (int)(units < sms ? units : sms);
-    attn_fwd_sm103_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn_fwd_sm103_kernel<D>, mq, mk, mv, mo, a) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH;
+    }
+    return ATTN_OK;
 }
 
 }  // namespace
