@@ -194,16 +194,17 @@ __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
 // atomic on the start-up path) and hands it to the MMA and softmax roles in order.
 // Index >= total means no work is left.
 struct UnitRing {
-    uint64_t* bars;
+    uint64_t* full;      // [kUnitRing] the producer has written the slot (1 arrival)
+    uint64_t* empty;     // [kUnitRing] every reader has read it (kUnitReaders arrivals)
     volatile int* idx;   // [kUnitRing]
     // reader side: the r-th unit index of this CTA, or false if a wait failed
     __device__ __forceinline__ bool get(int r, int& k, uint64_t lim, volatile int* abort_flag) const {
         const int sl = r % kUnitRing;
-        if (!wait_or_abort(&bars[kBarUnitFull + sl], (uint32_t)((r / kUnitRing) & 1), lim, abort_flag)) return false;
+        if (!wait_or_abort(&full[sl], (uint32_t)((r / kUnitRing) & 1), lim, abort_flag)) return false;
         k = idx[sl];
         return true;
     }
-    __device__ __forceinline__ void release(int r) const { mbar_arrive(&bars[kBarUnitEmpty + r % kUnitRing]); }
+    __device__ __forceinline__ void release(int r) const { mbar_arrive(&empty[r % kUnitRing]); }
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -613,6 +614,15 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 alpha = ex2(m_ref - m_tile);
                 m_ref = m_tile;
             }
+            const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const uint64_t negm2 = f2_pack(negm, negm);
+            uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
+            // keys 0-63 into tensor memory; the MMA takes them (and then computes the
+            // next block's scores) while keys 64-127 are being exponentiated
+            if (need_mask) p_lo_to_tmem<true>(sr, c2, negm2, acc, lim, tS);
+            else p_lo_to_tmem<false>(sr, c2, negm2, acc, lim, tS);
+            // Rescale O_t after the first half of the exponentials, so the wait for
+            // the previous block's PV_hi overlaps them; it must land before PV_lo(i).
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 if (pb_pending) {
                     if (!wait_warp(pb_done, pb_phase)) { ok = false; break; }
@@ -629,13 +639,6 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                     tmem_st32(tO + ch * 32, orow);
                 }
             }
-            const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t negm2 = f2_pack(negm, negm);
-            uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
-            // keys 0-63 into tensor memory; the MMA takes them (and then computes the
-            // next block's scores) while keys 64-127 are being exponentiated
-            if (need_mask) p_lo_to_tmem<true>(sr, c2, negm2, acc, lim, tS);
-            else p_lo_to_tmem<false>(sr, c2, negm2, acc, lim, tS);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_half);
@@ -711,7 +714,8 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
-    const UnitRing ring{bars, reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
+    const UnitRing ring{bars + kBarUnitFull, bars + kBarUnitEmpty,
+                        reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
@@ -790,6 +794,14 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
     }
 }
+}  // namespace
+}  // namespace bos
+
+#include "attn_fwd_d64.cuh"
+
+namespace bos {
+namespace {
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -830,7 +842,8 @@ std::atomic<unsigned int> g_sched_next{0};
 
 template <int D>
 int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
-    using C = Cfg<D>;
+    constexpr int kSmemBytes = (D == 64) ? d64::Cfg::kSmemBytes : Cfg<128>::kSmemBytes;
+    auto* const kernel = (D == 64) ? attn_fwd_d64_kernel : attn_fwd_sm103_kernel<128>;
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return ATTN_ERR_CUDA;
     const int BH = p.B * p.H;
@@ -861,8 +874,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
         if (dev >= 0 && dev < 64) sched_cache[dev] = sched;
     }
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        if (cudaFuncSetAttribute(attn_fwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_LAUNCH;
         }
@@ -884,14 +896,14 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, attn_fwd_sm103_kernel<D>, mq, mk, mv, mo, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, a) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_LAUNCH;
     }
