@@ -36,7 +36,8 @@ int validate_host(const void* q, const void* k, const void* v, const void* o, co
     const int64_t units = (int64_t)B * H * ((N + 255) / 256);   // 256-row work units
     if ((int64_t)B * H > INT_MAX || rows > ((int64_t)1 << 40) || units > INT_MAX / 2)
         return ATTN_ERR_BAD_SHAPE;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_D;
+    // a multiple of 8 (rows of Q, K, V, O must be 16-byte strided for TMA) up to 128
+    if (d < 8 || d > 128 || d % 8 != 0) return ATTN_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return ATTN_ERR_BAD_SCALE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_ARG;
     if (device_ptrs) {
@@ -120,7 +121,7 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_NULLPTR: return "a required pointer is NULL";
         case ATTN_ERR_BAD_SHAPE: return "B, H and N must be >= 1 and the sizes must fit the index space";
-        case ATTN_ERR_UNSUPPORTED_D: return "head dimension d must be 64 or 128";
+        case ATTN_ERR_UNSUPPORTED_D: return "head dimension d must be a multiple of 8 from 8 to 128";
         case ATTN_ERR_BAD_SCALE: return "scale must be finite";
         case ATTN_ERR_MISALIGNED: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";
         case ATTN_ERR_UNSUPPORTED_DEVICE: return "the current device is not compute capability 10.3 (sm_103a)";

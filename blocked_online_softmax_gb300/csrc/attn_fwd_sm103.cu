@@ -824,11 +824,12 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); boxes of 64 columns x
-// `rows` rows, 128-byte swizzle; loads read rows past N as zero, stores drop them.
-bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH, int N, int D, int rows) {
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); boxes of 64 columns x
+// `rows` rows, 128-byte swizzle; loads read rows past N (and columns past d) as
+// zero, stores drop them.
+bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH, int N, int d, int rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
@@ -849,8 +850,10 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     const int BH = p.B * p.H;
     CUtensorMap mq, mk, mv, mo;
     // Q, K and V move in 128-row boxes; O is stored 32 rows (one warp) at a time
-    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, D, kBM) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, D, kBN) ||
-        !encode_qkv_map(enc, &mv, p.v, BH, p.N, D, kBN) || !encode_qkv_map(enc, &mo, p.o, BH, p.N, D, 32))
+    // (the maps describe the caller's d columns; boxes are 64 wide, so columns
+    // from d up to the kernel's width D load as zero and are not stored)
+    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, p.d, kBM) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, p.d, kBN) ||
+        !encode_qkv_map(enc, &mv, p.v, BH, p.N, p.d, kBN) || !encode_qkv_map(enc, &mo, p.o, BH, p.N, p.d, 32))
         return ATTN_ERR_BAD_SHAPE;
     static int sms_cache[64] = {0};
     static int attr_done[64] = {0};
@@ -913,7 +916,9 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
 }  // namespace
 
 int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev) {
-    return p.d == 64 ? launch_d<64>(p, stream, dev) : launch_d<128>(p, stream, dev);
+    // head dims below a kernel's width run on it with the missing columns
+    // zero-filled by TMA on load and clipped on store
+    return p.d <= 64 ? launch_d<64>(p, stream, dev) : launch_d<128>(p, stream, dev);
 }
 
 void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs; }

@@ -55,7 +55,8 @@ def _call(lib, q=16, k=32, v=48, o=64, lse=80, B=1, H=1, N=8, d=64, scale=0.125,
     (dict(q=0), bos.ATTN_ERR_NULLPTR), (dict(lse=0), bos.ATTN_ERR_NULLPTR),
     (dict(B=0), bos.ATTN_ERR_BAD_SHAPE), (dict(H=-1), bos.ATTN_ERR_BAD_SHAPE),
     (dict(N=0), bos.ATTN_ERR_BAD_SHAPE), (dict(B=1 << 20, H=1 << 20), bos.ATTN_ERR_BAD_SHAPE),
-    (dict(d=96), bos.ATTN_ERR_UNSUPPORTED_D), (dict(d=0), bos.ATTN_ERR_UNSUPPORTED_D),
+    (dict(d=60), bos.ATTN_ERR_UNSUPPORTED_D), (dict(d=0), bos.ATTN_ERR_UNSUPPORTED_D),
+    (dict(d=136), bos.ATTN_ERR_UNSUPPORTED_D), (dict(d=4), bos.ATTN_ERR_UNSUPPORTED_D),
     (dict(scale=float("nan")), bos.ATTN_ERR_BAD_SCALE), (dict(scale=float("inf")), bos.ATTN_ERR_BAD_SCALE),
     (dict(causal=2), bos.ATTN_ERR_BAD_ARG),
     (dict(q=17), bos.ATTN_ERR_MISALIGNED), (dict(o=72), bos.ATTN_ERR_MISALIGNED),
@@ -68,7 +69,7 @@ def test_host_validation_before_any_launch(lib, kw, code):
 def test_host_entry_validation(lib):
     st = lib.attn_fwd_host(None, 8, 8, 8, 8, 1, 1, 4, 64, ctypes.c_float(1.0), 0, None)
     assert st == bos.ATTN_ERR_NULLPTR
-    st = lib.attn_fwd_host(8, 8, 8, 8, 8, 1, 1, 4, 80, ctypes.c_float(1.0), 0, None)
+    st = lib.attn_fwd_host(8, 8, 8, 8, 8, 1, 1, 4, 81, ctypes.c_float(1.0), 0, None)
     assert st == bos.ATTN_ERR_UNSUPPORTED_D
 
 

@@ -79,13 +79,58 @@ def test_several_tiles_ragged_tail(d, causal):
     assert_parity(o, lse, o_ref, lse_ref, f"B2H3N1000 d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [8, 16, 32, 48, 72, 80, 96, 112, 120])
+def test_other_head_dims(d, causal):
+    """Head dims below a kernel's width: the missing columns load as zero and are never stored."""
+    q, k, v = make_qkv(1, 2, 300, d, seed=300 + d)
+    scale = float(np.float32(d ** -0.5))
+    o, lse = run_guarded(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    assert_parity(o, lse, o_ref, lse_ref, f"N=300 d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("mult", [4.0, 8.0])
 @pytest.mark.parametrize("causal", [False, True])
-def test_large_logits_stability(mult, causal):
-    q, k, v = make_qkv(1, 2, 700, 64, seed=5, logit_mult=mult)
+def test_large_logits_stability(mult, causal, d):
+    """Logits of tens of log2 units: the running max moves often and O is rescaled in tensor memory."""
+    q, k, v = make_qkv(1, 2, 700, d, seed=5 + d, logit_mult=mult)
     o, lse = run_guarded(q, k, v, 0.125, causal)
     o_ref, lse_ref = oracle.attention(q, k, v, 0.125, causal)
-    assert_parity(o, lse, o_ref, lse_ref, f"x{mult} causal={causal}")
+    assert_parity(o, lse, o_ref, lse_ref, f"x{mult} d={d} causal={causal}")
+
+
+def test_back_to_back_dependency():
+    """A launch that reads the previous launch's output on the same stream sees all of it.
+
+    Call A has V = 1, so its O is 1: O = P V / l with l the sum of the probabilities,
+    off only by the bf16 rounding of P (relative 2^-9), so within one bf16 step of 1.
+    Call B uses that O as its V, so its O is within a step of 1 as well; A's and B's
+    O buffers start out as sentinels (-12288), so reading A's output early would show.
+    """
+    dev = torch.device("cuda")
+    B, H, N, d = 2, 16, 4096, 128
+    qa, ka, _ = make_qkv(B, H, N, d, seed=21)
+    qa, ka = qa.to(dev), ka.to(dev)
+    va = torch.ones(B, H, N, d, dtype=torch.bfloat16, device=dev)
+    oa = torch.full((B, H, N, d), SENT_BF16, dtype=torch.bfloat16, device=dev)
+    la = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    qb, kb, _ = make_qkv(1, 4, N, d, seed=22)
+    qb, kb = qb.to(dev), kb.to(dev)
+    ob = torch.full((1, 4, N, d), SENT_BF16, dtype=torch.bfloat16, device=dev)
+    lb = torch.empty(1, 4, N, dtype=torch.float32, device=dev)
+    scale = float(np.float32(d ** -0.5))
+    for _ in range(3):
+        oa.fill_(SENT_BF16)
+        ob.fill_(SENT_BF16)
+        bos.attn_fwd(qa, ka, va, oa, la, B, H, N, d, scale, 1, None)
+        vb = oa[0, :4]                            # A's first 4 heads, written by A
+        bos.attn_fwd(qb, kb, vb, ob, lb, 1, 4, N, d, scale, 1, None)
+        torch.cuda.synchronize()
+        assert torch.all((oa.float() - 1.0).abs() <= 2.0 ** -8), "O of V = 1 must be 1"
+        assert torch.all((ob.float() - 1.0).abs() <= 2.0 ** -8), \
+            "the second launch read its V before the first launch wrote it"
 
 
 def test_scale_zero_and_negative():
