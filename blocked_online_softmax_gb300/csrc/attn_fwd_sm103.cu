@@ -105,7 +105,7 @@ struct Cfg {
     // K/V ring depth. V_i's stage stays busy until the PV of keys 64-127, which a
     // stream issues after S(i+1); with four 32 KB stages (d = 128) every load has
     // about a block of lead.
-    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kStages = 4;
     static constexpr int kBoxes = D / 64;                   // 64-column TMA boxes per tile
     // shared memory: Q tiles [2] | second halves of P [2] | K/V ring | barriers | misc
     static constexpr int kOffPb = 2 * kTileBytes;
@@ -663,14 +663,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         const float l_safe = (l > 0.f) ? l : 1.f;
         const float inv = 1.f / l_safe;
         uint32_t ov[D];
-        if constexpr (D == 128) {
-            tmem_ld128(tO, ov);
-        } else {
-            uint32_t (&h0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[0]);
-            uint32_t (&h1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[32]);
-            tmem_ld32(tO, h0);
-            tmem_ld32(tO + 32, h1);
-        }
+        tmem_ld128(tO, ov);
         tc_fence_before();
 #pragma unroll
         for (int s = 0; s < C::kBoxes; ++s) {
@@ -700,11 +693,13 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
 
 // ------------------------------------------------------------------ kernel
 
+// Instantiated for D = 128 only; head dims up to 64 run on attn_fwd_d64_kernel.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const KernelArgs a) {
+    static_assert(D == 128, "the d = 64 path is attn_fwd_d64_kernel");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
