@@ -200,8 +200,14 @@ def time_oracle(w, q, k, v, target_seconds):
     oracle.attention(q, k, v, w.scale, w.causal, rows=probe)
     dt = max(time.perf_counter() - t0, 1e-6)
     per_flop = dt / oracle_rows_flops(w, probe)
-    # grow the sample to about target_seconds; whole heads first, then strided rows of one head
     head_flops = oracle_rows_flops(w, np.arange(w.N))
+    if head_flops * per_flop < 4.0 * target_seconds:
+        # a few rows overstate the cost per FLOP (thread start-up, uneven rows):
+        # re-estimate on one whole head when that is cheap
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.scale, w.causal, rows=np.arange(w.N, dtype=np.int64))
+        per_flop = max(time.perf_counter() - t0, 1e-6) / head_flops
+    # grow the sample to about target_seconds; whole heads first, then strided rows of one head
     n_heads = int(max(0, min(w.B * w.H, target_seconds / (per_flop * head_flops))))
     if n_heads >= 1:
         rows = np.arange(n_heads * w.N, dtype=np.int64)
