@@ -336,6 +336,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         tmem_ld32(tO, h0);
         tmem_ld32(tO + 32, h1);
         tc_fence_before();
+        if (lane == 0) bulk_wait_read0();   // the previous unit's store has read the staging rows
+        __syncwarp();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {     // 16-byte chunk = 8 output columns
             const int col = q * 8;
@@ -348,10 +350,9 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {   // this warp's 32 rows; the buffer is rewritten only after the store has read it
+        if (lane == 0) {   // this warp's 32 rows; the next epilogue waits for the read
             tma_store_3d(tm_o, ewarp, 0, tile_row0 + wq * 32, u.bh);
             bulk_commit();
-            bulk_wait_read0();
         }
         __syncwarp();
         if (row < a.N) a.lse[(int64_t)u.bh * a.N + row] = (m_ref + log2f(l_safe)) * 0.69314718055994531f;

@@ -563,6 +563,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
     const uint64_t c2 = f2_pack(c, c);
     const int total = a.BH * a.U;
     uint32_t s_phase = 0, pb_phase = 0;
+    bool store_pending = false;   // an O store of this warp may still be reading the P buffer
     bool ok = true;
     // bounded wait shared by the whole warp
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -646,6 +647,11 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 if (!wait_warp(pb_done, pb_phase)) { ok = false; break; }
                 pb_phase ^= 1;
             }
+            if (store_pending) {   // the previous unit's O stores must have read this buffer
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+                store_pending = false;
+            }
             if (need_mask) p_hi_to_smem<true>(sr, c2, negm2, acc, lim, prow, swz);
             else p_hi_to_smem<false>(sr, c2, negm2, acc, lim, prow, swz);
             fence_proxy_async_smem();
@@ -667,6 +673,10 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         tc_fence_before();
 #pragma unroll
         for (int s = 0; s < C::kBoxes; ++s) {
+            if (s > 0) {   // the previous slice's store must have read the buffer
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {     // 16-byte chunk = 8 output columns
                 const int col = s * 64 + q * 8;
@@ -679,13 +689,13 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {   // this warp's 32 rows; the buffer is rewritten only after the store has read it
+            if (lane == 0) {   // this warp's 32 rows
                 tma_store_3d(tm_o, pwarp, s * 64, tile_row0 + wq * 32, u.bh);
                 bulk_commit();
-                bulk_wait_read0();
             }
             __syncwarp();
         }
+        store_pending = true;   // the last slice's read is waited for before the buffer is next written
         if (row < a.N) a.lse[(int64_t)u.bh * a.N + row] = (m_ref + log2f(l_safe)) * 0.69314718055994531f;
     }
     if (lane == 0) bulk_wait0();   // this warp's O stores are complete
