@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle sample time")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--op", choices=("attention", "softmax"), default="attention",
+                    help="attention (the default hot path) or the fused row softmax (a memory-bound workload)")
+    ap.add_argument("--softmax-shape", default="32768x4096", help="rows x cols of the --op softmax matrix (fp32)")
     return ap.parse_args()
 
 
@@ -276,7 +279,6 @@ def workload_config(w):
 
 
 def run_ours(args, w):
-    import numpy as np
     import torch
 
     import blocked_online_softmax_gb300 as bos
@@ -404,8 +406,84 @@ def run_ours(args, w):
     return 0
 
 
+SOFTMAX_SOURCES = ("blocked_online_softmax_gb300/csrc/softmax_rows.cu",)
+
+
+def run_softmax(args):
+    """The fused row softmax on one GPU: GB/s against the measured HBM copy bandwidth.
+
+    Algorithmic bytes: one read and one write of the fp32 matrix (rows that fit
+    on chip), or two reads and one write (the online two-pass path). The matrix
+    is larger than L2, so the K launches run back to back between two events.
+    """
+    import torch
+
+    import blocked_online_softmax_gb300 as bos
+    rows, cols = (int(v) for v in args.softmax_shape.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator().manual_seed(11)
+    x_h = torch.randn(rows, cols, generator=g)
+    x = x_h.to(dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    passes = 2 if cols <= 16384 else 3
+    nbytes = float(passes) * rows * cols * 4
+    for _ in range(max(3, args.warmup)):
+        bos.softmax_rows_fwd(x, y, rows, cols, cols, cols, stream)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    sampler.mark()
+    t_begin.record(stream)
+    for _ in range(args.steps):
+        bos.softmax_rows_fwd(x, y, rows, cols, cols, cols, stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    gbs = nbytes * args.steps / (total_ms / 1e3) / 1e9
+    peaks, peaks_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    h = hashlib.sha256()
+    for rel in SOFTMAX_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        xs = x_h.numpy()
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 10.0) and done < rows:
+            oracle.softmax_rows(xs[done:done + 64])
+            done += 64
+        dt = time.perf_counter() - t0
+        cpu = {"value": 2.0 * done * cols * 4 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {done} rows of the same matrix; fp64 three-pass softmax per row; {dt:.2f} s"}
+    line = {"metric": "fused row softmax GB/s on 1 GB300 (fp32)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"row softmax fp32 {rows}x{cols}", "rows": rows, "cols": cols,
+                       "l2": f"matrix {rows * cols * 4 / 1e6:.0f} MB read + written per step (> 129 MB L2), no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "peak_kind": f"{peaks_kind} copy bandwidth",
+                         "kernel": "softmax_rows_fwd", "algorithmic_bytes": nbytes,
+                         "mean_launch_ms": total_ms / args.steps},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clocks,
+            "kernel_source_sha": h.hexdigest()[:16]}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "softmax":
+        return run_softmax(args)
     from blocked_online_softmax_gb300.workloads import BY_NAME
     if args.workload not in BY_NAME:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(BY_NAME)}")

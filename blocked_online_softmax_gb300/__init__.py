@@ -5,9 +5,9 @@ library ``libbos_attn.so`` built from ``csrc/`` (see ``include/attn.h`` for the
 contract). There is no CPU or PyTorch fallback: if the library is missing or
 the GPU is not sm_103a, the calls raise.
 
-Names follow the C ABI: ``attn_fwd``, ``attn_fwd_host``, ``attn_status_string``.
-``attention`` is a convenience that allocates O and LSE with torch (device
-memory only) and calls ``attn_fwd``.
+Names follow the C ABI: ``attn_fwd``, ``attn_fwd_host``, ``attn_status_string``,
+``softmax_rows_fwd``. ``attention`` and ``softmax`` are conveniences that
+allocate their outputs with torch (device memory only) and call the C entry.
 """
 from __future__ import annotations
 
@@ -36,7 +36,8 @@ ATTN_ERR_TOO_LARGE = 11
 
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
-                    "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version")
+                    "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version",
+                    "softmax_rows_fwd")
 
 _lib = None
 
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_status_string.argtypes = [i]
     lib.attn_abi_version.restype = i
     lib.attn_abi_version.argtypes = []
+    lib.softmax_rows_fwd.restype = i
+    lib.softmax_rows_fwd.argtypes = [vp, vp, i, i, ctypes.c_longlong, ctypes.c_longlong, vp]
     _lib = lib
     return lib
 
@@ -156,6 +159,26 @@ def attn_set_wait_limit_ns(ns: int) -> None:
 def attn_set_test_stall(on: bool) -> None:
     """Test hook: make every launch's MMA thread wait on a barrier nothing signals."""
     load_library().attn_set_test_stall(int(bool(on)))
+
+
+def softmax_rows_fwd(x, y, rows: int, cols: int, x_row_stride: int, y_row_stride: int, stream=None) -> None:
+    """Row softmax of an fp32 device matrix (C ``softmax_rows_fwd``); strides in elements."""
+    lib = load_library()
+    st = lib.softmax_rows_fwd(_ptr(x), _ptr(y), int(rows), int(cols), int(x_row_stride), int(y_row_stride),
+                              _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "softmax_rows_fwd")
+
+
+def softmax(x, out=None, stream=None):
+    """Softmax over the last dimension of a 2-D fp32 CUDA tensor (rows may be strided)."""
+    import torch
+    if x.dim() != 2 or x.dtype != torch.float32 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D fp32 CUDA tensor with unit column stride")
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    softmax_rows_fwd(x, out, x.shape[0], x.shape[1], x.stride(0), out.stride(0), stream)
+    return out
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None):

@@ -15,6 +15,7 @@
 
 #include "attn.h"
 #include "attn_internal.h"
+#include "softmax_rows.h"
 
 namespace {
 
@@ -97,6 +98,20 @@ extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, 
     p.B = B; p.H = H; p.N = N; p.d = d;
     p.scale = scale; p.causal = causal;
     return bos::host_forward(p, static_cast<cudaStream_t>(stream_), dev);
+}
+
+extern "C" int softmax_rows_fwd(const float* x, float* y, int rows, int cols, long long x_row_stride,
+                                long long y_row_stride, void* stream) {
+    if (!x || !y) return ATTN_ERR_NULLPTR;
+    if (rows < 1 || cols < 1 || x_row_stride < cols || y_row_stride < cols) return ATTN_ERR_BAD_SHAPE;
+    if ((long long)rows > (LLONG_MAX / 4) / x_row_stride || (long long)rows > (LLONG_MAX / 4) / y_row_stride)
+        return ATTN_ERR_BAD_SHAPE;
+    if (!aligned(x, 4) || !aligned(y, 4)) return ATTN_ERR_MISALIGNED;
+    int dev = 0;
+    const int st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+    return bos::launch_softmax_rows(x, y, rows, cols, x_row_stride, y_row_stride, static_cast<cudaStream_t>(stream),
+                                    dev);
 }
 
 extern "C" int attn_device_status(void* stream) {

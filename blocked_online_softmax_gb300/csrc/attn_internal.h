@@ -38,4 +38,8 @@ void set_test_stall(int on);
 // clears it.
 int read_and_clear_device_status(cudaStream_t stream);
 
+// Row softmax (softmax_rows_fwd) for validated arguments on `stream`.
+int launch_softmax_rows(const float* x, float* y, int rows, int cols, long long x_stride, long long y_stride,
+                        cudaStream_t stream, int dev);
+
 }  // namespace bos

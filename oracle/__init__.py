@@ -123,3 +123,19 @@ def softmax_row(x):
     dp = ctypes.POINTER(ctypes.c_double)
     lse = _load().oracle_softmax_row_f64(xa.ctypes.data_as(dp), xa.size, p.ctypes.data_as(dp))
     return p, float(lse)
+
+
+def softmax_rows(x):
+    """Row softmax of a 2-D array, in fp64: every row through softmax_row.
+
+    This is the definition the fused-softmax kernel computes ("4.4 Writing GPU
+    Kernels with Triton", Kernel 2 "Fused Softmax"; "Triton", fused softmax):
+    y[i, j] = exp(x[i, j] - max_k x[i, k]) / sum_k exp(x[i, k] - max_k x[i, k]).
+    """
+    xa = np.asarray(x, dtype=np.float64)
+    if xa.ndim != 2:
+        raise ValueError("softmax_rows takes a 2-D array")
+    out = np.empty_like(xa)
+    for i in range(xa.shape[0]):
+        out[i], _ = softmax_row(xa[i])
+    return out

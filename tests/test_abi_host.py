@@ -25,7 +25,7 @@ def _declared_functions():
             continue
         text = open(os.path.join(ROOT, "include", path)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:attn|softmax)_\w+)\s*\(", text, flags=re.M)
     return names
 
 
