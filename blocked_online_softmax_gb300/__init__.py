@@ -37,7 +37,7 @@ ATTN_ERR_TOO_LARGE = 11
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
                     "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version",
-                    "softmax_rows_fwd")
+                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes")
 
 _lib = None
 
@@ -74,6 +74,10 @@ def load_library(path: str = LIB_PATH):
     lib.attn_abi_version.argtypes = []
     lib.softmax_rows_fwd.restype = i
     lib.softmax_rows_fwd.argtypes = [vp, vp, i, i, ctypes.c_longlong, ctypes.c_longlong, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, vp]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     _lib = lib
     return lib
 
@@ -159,6 +163,34 @@ def attn_set_wait_limit_ns(ns: int) -> None:
 def attn_set_test_stall(on: bool) -> None:
     """Test hook: make every launch's MMA thread wait on a barrier nothing signals."""
     load_library().attn_set_test_stall(int(bool(on)))
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Device workspace bytes ``attn_bwd`` needs (C ``attn_bwd_workspace_bytes``)."""
+    return int(load_library().attn_bwd_workspace_bytes(int(B), int(H), int(N), int(d)))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes: int, B: int, H: int, N: int, d: int,
+             scale: float, causal, stream=None) -> None:
+    """Enqueue the backward pass (C ``attn_bwd``); raises AttnError on a nonzero status."""
+    st = load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(workspace), int(workspace_bytes), int(B), int(H), int(N), int(d),
+                                 float(scale), int(causal), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+
+
+def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, stream=None):
+    """dq, dk, dv (bf16) for the attention() forward outputs o, lse and the gradient dout."""
+    import torch
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = attn_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, nbytes, B, H, N, d, scale, causal, stream)
+    return dq, dk, dv
 
 
 def softmax_rows_fwd(x, y, rows: int, cols: int, x_row_stride: int, y_row_stride: int, stream=None) -> None:

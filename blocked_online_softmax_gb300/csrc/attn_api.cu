@@ -100,6 +100,34 @@ extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, 
     return bos::host_forward(p, static_cast<cudaStream_t>(stream_), dev);
 }
 
+extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+    static const char one = 0;
+    if (validate_host(&one, &one, &one, &one, reinterpret_cast<const float*>(&one), B, H, N, d, 1.0f, 0, false) !=
+        ATTN_OK)
+        return 0;
+    return bos::attn_bwd_workspace(B, H, N, d);
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        int B, int H, int N, int d, float scale, int causal, void* stream) {
+    int st = validate_host(q, k, v, dq, lse, B, H, N, d, scale, causal, true);
+    if (st != ATTN_OK) return st;
+    if (!o || !dout || !dk || !dv || !workspace) return ATTN_ERR_NULLPTR;
+    if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
+        return ATTN_ERR_MISALIGNED;
+    if (workspace_bytes < bos::attn_bwd_workspace(B, H, N, d)) return ATTN_ERR_BAD_ARG;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+    bos::AttnBwdParams p;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.workspace = workspace;
+    p.B = B; p.H = H; p.N = N; p.d = d;
+    p.scale = scale; p.causal = causal;
+    return bos::launch_attn_bwd(p, static_cast<cudaStream_t>(stream), dev);
+}
+
 extern "C" int softmax_rows_fwd(const float* x, float* y, int rows, int cols, long long x_row_stride,
                                 long long y_row_stride, void* stream) {
     if (!x || !y) return ATTN_ERR_NULLPTR;

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 namespace bos {
@@ -37,6 +38,28 @@ void set_test_stall(int on);
 // Synchronises `stream`, returns the sticky device status (an attn_status) and
 // clears it.
 int read_and_clear_device_status(cudaStream_t stream);
+
+struct AttnBwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const void* dout;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    void* workspace;     // fp32 dQ accumulator [B,H,N,d], then fp32 D [B,H,N]
+    int B, H, N, d;
+    float scale;
+    int causal;
+};
+
+// Bytes of workspace attn_bwd needs (each part 256-byte aligned).
+size_t attn_bwd_workspace(int B, int H, int N, int d);
+
+// Enqueues the backward pass (preprocess, main kernel, dQ cast) for validated arguments.
+int launch_attn_bwd(const AttnBwdParams& p, cudaStream_t stream, int dev);
 
 // Row softmax (softmax_rows_fwd) for validated arguments on `stream`.
 int launch_softmax_rows(const float* x, float* y, int rows, int cols, long long x_stride, long long y_stride,

@@ -159,6 +159,37 @@ const char* attn_status_string(int status);
 /* Version of this ABI (incremented on any incompatible change). */
 int attn_abi_version(void);
 
+/*
+ * Backward pass of attn_fwd: Kernel 5 "FlashAttention Backward" of "4.4 Writing
+ * GPU Kernels with Triton" (llm-stack-book). With P = exp(scale * q k^T - LSE)
+ * rebuilt from the forward's natural-log LSE, D = rowsum(dO * O) and
+ * dS = P * (dO v^T - D) * scale:
+ *
+ *     dq = dS k,   dk = dS^T q,   dv = P^T dO.
+ *
+ *   q, k, v, o, dout : bf16, contiguous [B, H, N, d], device memory, 16-byte
+ *                      aligned; o and lse are attn_fwd's outputs for the same
+ *                      q, k, v, scale and causal; dout is dL/dO.
+ *   lse              : fp32 [B, H, N], device memory, 4-byte aligned.
+ *   dq, dk, dv       : bf16 [B, H, N, d] outputs, 16-byte aligned.
+ *   workspace        : device memory of workspace_bytes >=
+ *                      attn_bwd_workspace_bytes(B, H, N, d), 256-byte aligned:
+ *                      the fp32 dq accumulator (every key block adds its part
+ *                      with atomic adds) and the fp32 row sums D. Owned by the
+ *                      caller; nothing is allocated.
+ *   B, H, N, d, scale, causal, stream: as attn_fwd.
+ *
+ * Asynchronous on stream. Returns the attn_fwd validation codes, or
+ * ATTN_ERR_BAD_ARG when the workspace is smaller than needed; on an error
+ * nothing is launched or written.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+             float scale, int causal, void* stream);
+
+/* Workspace bytes attn_bwd needs for these sizes (0 if B, H, N or d are out of range). */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
 #ifdef __cplusplus
 }
 #endif

@@ -125,6 +125,48 @@ def softmax_row(x):
     return p, float(lse)
 
 
+def attention_bwd(q, k, v, do, scale: float, causal: bool):
+    """dq, dk, dv in fp64 for inputs shaped [B,H,N,d] (bf16 tensors or float arrays) and dO.
+
+    The definition the backward pass computes ("4.4 Writing GPU Kernels with
+    Triton", Kernel 5 "FlashAttention Backward"), per (batch, head), with the
+    score matrix materialised: S = scale q k^T (causal: -inf above the
+    diagonal), P = softmax(S) by rows, O = P v, dv = P^T dO, dP = dO v^T,
+    D = rowsum(dO * O), dS = P * (dP - D), dq = scale dS k, dk = scale dS^T q.
+    """
+    qa, ka, va, ga = (_to_f64(t) for t in (q, k, v, do))
+    B, H, N, d = qa.shape
+    dq = np.zeros_like(qa)
+    dk = np.zeros_like(ka)
+    dv = np.zeros_like(va)
+    mask = np.tril(np.ones((N, N), dtype=bool)) if causal else None
+    for b in range(B):
+        for h in range(H):
+            Q, K, V, G = qa[b, h], ka[b, h], va[b, h], ga[b, h]
+            S = scale * (Q @ K.T)
+            if mask is not None:
+                S = np.where(mask, S, -np.inf)
+            P = np.exp(S - S.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            O = P @ V
+            dv[b, h] = P.T @ G
+            dP = G @ V.T
+            Dr = (G * O).sum(axis=1, keepdims=True)
+            dS = P * (dP - Dr)
+            dq[b, h] = scale * (dS @ K)
+            dk[b, h] = scale * (dS.T @ Q)
+    return dq, dk, dv
+
+
+def _to_f64(t):
+    """bf16 torch tensor or array -> float64 numpy array (bf16 widened exactly)."""
+    if hasattr(t, "dtype") and str(getattr(t, "dtype", "")).endswith("bfloat16"):
+        return t.detach().to("cpu").float().numpy().astype(np.float64)
+    if hasattr(t, "detach"):
+        return t.detach().to("cpu").numpy().astype(np.float64)
+    return np.asarray(t, dtype=np.float64)
+
+
 def softmax_rows(x):
     """Row softmax of a 2-D array, in fp64: every row through softmax_row.
 

@@ -1,0 +1,72 @@
+"""Pins of the backward oracle (no GPU): it is the derivative of the forward oracle.
+
+The forward oracle is pinned separately (test_oracle_pins.py); here central
+finite differences of L = sum(O * dO) through that forward, in fp64, must match
+the closed-form gradients, and special cases with known answers hold.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    oracle.build()
+
+
+def _loss(q, k, v, g, scale, causal):
+    o, _ = oracle.attention(q, k, v, scale, causal)
+    return float((o * g).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_finite_differences(causal):
+    rng = np.random.default_rng(5 + causal)
+    B, H, N, d = 1, 2, 5, 3
+    q, k, v, g = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    scale = 0.7
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, scale, causal)
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = dict(q=q, k=k, v=v)
+            args_m = dict(q=q, k=k, v=v)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (_loss(args_p["q"], args_p["k"], args_p["v"], g, scale, causal)
+                        - _loss(args_m["q"], args_m["k"], args_m["v"], g, scale, causal)) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-8, err_msg=f"d{name}")
+
+
+def test_identical_keys_give_zero_dq():
+    """Equal keys make every score row constant in q: dq = 0 (and dS sums to 0 per row)."""
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((1, 1, 6, 4))
+    k = np.broadcast_to(rng.standard_normal((1, 1, 1, 4)), (1, 1, 6, 4)).copy()
+    v, g = rng.standard_normal((2, 1, 1, 6, 4))
+    dq, _, _ = oracle.attention_bwd(q, k, v, g, 0.5, False)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+
+
+def test_constant_values_give_zero_dq_dk():
+    """Equal value rows make O independent of the scores: dq = dk = 0, dv = P^T dO."""
+    rng = np.random.default_rng(7)
+    q, k, g = rng.standard_normal((3, 1, 2, 7, 4))
+    v = np.broadcast_to(rng.standard_normal((1, 1, 1, 4)), (1, 2, 7, 4)).copy()
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, 0.3, True)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-13)
+
+
+def test_uniform_attention_dv_is_mean_of_do():
+    """q = 0: every row attends uniformly, so dv_j = sum_i dO_i / N (non-causal)."""
+    rng = np.random.default_rng(8)
+    N = 9
+    q = np.zeros((1, 1, N, 4))
+    k, v, g = rng.standard_normal((3, 1, 1, N, 4))
+    _, _, dv = oracle.attention_bwd(q, k, v, g, 1.0, False)
+    np.testing.assert_allclose(dv[0, 0], np.broadcast_to(g[0, 0].sum(axis=0) / N, (N, 4)), rtol=1e-13)
