@@ -50,8 +50,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle sample time")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--op", choices=("attention", "softmax"), default="attention",
-                    help="attention (the default hot path) or the fused row softmax (a memory-bound workload)")
+    ap.add_argument("--op", choices=("attention", "softmax", "backward"), default="attention",
+                    help="attention (the default hot path), the fused row softmax (a memory-bound workload), "
+                         "or the attention backward pass")
     ap.add_argument("--softmax-shape", default="32768x4096", help="rows x cols of the --op softmax matrix (fp32)")
     return ap.parse_args()
 
@@ -492,6 +493,67 @@ def run_softmax(args):
     return 0
 
 
+def run_backward(args, w):
+    """The attention backward pass (attn_bwd) on one GPU, on the chosen workload.
+
+    FLOPs counted: five 2*N*N*d products per (batch, head) (S, dP, dV, dK, dQ),
+    i.e. 10*B*H*N^2*d, halved under causal masking (2.5x the forward count). The
+    timed step is the whole backward call (D preprocess, key-block kernel, dQ
+    cast); the forward outputs it needs are computed once before timing.
+    """
+    import torch
+
+    import blocked_online_softmax_gb300 as bos
+    from blocked_online_softmax_gb300.workloads import workload_qkv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q_h, k_h, v_h = workload_qkv(w)
+    g = torch.Generator().manual_seed(99)
+    do_h = torch.randn(q_h.shape, generator=g).to(torch.bfloat16)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o, lse = bos.attention(q, k, v, scale=w.scale, causal=w.causal)
+    nbytes = bos.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream()
+    step = lambda: bos.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, nbytes, w.B, w.H, w.N, w.d, w.scale,
+                                w.causal, stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    t_begin.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    flops = 2.5 * w.flops
+    tf = flops * args.steps / (total_ms / 1e3) / 1e12
+    peaks, peaks_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    line = {"metric": "attention bwd TFLOP/s on 1 GB300 (bf16)", "value": tf, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.describe().replace("attention fwd", "attention bwd"), "name": w.name, "B": w.B, "H": w.H, "N": w.N,
+                       "d": w.d, "causal": w.causal, "flops_per_step": flops,
+                       "l2": "inputs larger than L2, no flush" if 5 * w.B * w.H * w.N * w.d * 2 > 129e6
+                       else "inputs fit in L2, no flush"},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": UNIT, "frac": tf / peak,
+                         "traffic": None, "peak_kind": f"{peaks_kind} dense bf16 burst (cuBLAS)",
+                         "kernel": "attn_bwd (3 kernels per step)", "mean_launch_ms": total_ms / args.steps},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": 3 * args.steps, "clocks": clocks,
+            "kernel_source_sha": kernel_source_hash()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.op == "softmax":
@@ -500,6 +562,8 @@ def main():
     if args.workload not in BY_NAME:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(BY_NAME)}")
     w = BY_NAME[args.workload]
+    if args.op == "backward":
+        return run_backward(args, w)
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     if args.impl == "reference":
