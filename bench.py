@@ -516,7 +516,7 @@ def run_backward(args, w):
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream()
-    step = lambda: bos.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, nbytes, w.B, w.H, w.N, w.d, w.scale,
+    step = lambda: bos.attn_bwd(q, k, v, o, do, lse, None, dq, dk, dv, ws, nbytes, w.B, w.H, w.N, w.d, w.scale,
                                 w.causal, stream)
     for _ in range(max(3, args.warmup)):
         step()

@@ -75,7 +75,7 @@ def load_library(path: str = LIB_PATH):
     lib.softmax_rows_fwd.restype = i
     lib.softmax_rows_fwd.argtypes = [vp, vp, i, i, ctypes.c_longlong, ctypes.c_longlong, vp]
     lib.attn_bwd.restype = i
-    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, vp]
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, vp]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     _lib = lib
@@ -170,18 +170,20 @@ def attn_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().attn_bwd_workspace_bytes(int(B), int(H), int(N), int(d)))
 
 
-def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes: int, B: int, H: int, N: int, d: int,
-             scale: float, causal, stream=None) -> None:
-    """Enqueue the backward pass (C ``attn_bwd``); raises AttnError on a nonzero status."""
-    st = load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+def attn_bwd(q, k, v, o, dout, lse, dlse, dq, dk, dv, workspace, workspace_bytes: int, B: int, H: int, N: int,
+             d: int, scale: float, causal, stream=None) -> None:
+    """Enqueue the backward pass (C ``attn_bwd``; dlse may be None); raises AttnError on a nonzero status."""
+    st = load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dlse), _ptr(dq),
+                                 _ptr(dk),
                                  _ptr(dv), _ptr(workspace), int(workspace_bytes), int(B), int(H), int(N), int(d),
                                  float(scale), int(causal), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
 
 
-def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, stream=None):
-    """dq, dk, dv (bf16) for the attention() forward outputs o, lse and the gradient dout."""
+def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, stream=None,
+                       dlse=None):
+    """dq, dk, dv (bf16) for the attention() forward outputs o, lse and the gradients dout (and dlse, optional)."""
     import torch
     B, H, N, d = q.shape
     if scale is None:
@@ -189,7 +191,10 @@ def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal
     nbytes = attn_bwd_workspace_bytes(B, H, N, d)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, nbytes, B, H, N, d, scale, causal, stream)
+    if dlse is not None:
+        if dlse.dtype != torch.float32 or not dlse.is_contiguous() or tuple(dlse.shape) != (B, H, N):
+            raise ValueError("dlse must be a contiguous fp32 [B,H,N] tensor")
+    attn_bwd(q, k, v, o, dout, lse, dlse, dq, dk, dv, ws, nbytes, B, H, N, d, scale, causal, stream)
     return dq, dk, dv
 
 

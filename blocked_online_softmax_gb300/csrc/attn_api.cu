@@ -109,19 +109,20 @@ extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                        const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        const float* lse, const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                         int B, int H, int N, int d, float scale, int causal, void* stream) {
     int st = validate_host(q, k, v, dq, lse, B, H, N, d, scale, causal, true);
     if (st != ATTN_OK) return st;
     if (!o || !dout || !dk || !dv || !workspace) return ATTN_ERR_NULLPTR;
-    if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
+    if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256) ||
+        !aligned(dlse, 4))
         return ATTN_ERR_MISALIGNED;
     if (workspace_bytes < bos::attn_bwd_workspace(B, H, N, d)) return ATTN_ERR_BAD_ARG;
     int dev = 0;
     st = check_device(&dev);
     if (st != ATTN_OK) return st;
     bos::AttnBwdParams p;
-    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse; p.dlse = dlse;
     p.dq = dq; p.dk = dk; p.dv = dv; p.workspace = workspace;
     p.B = B; p.H = H; p.N = N; p.d = d;
     p.scale = scale; p.causal = causal;

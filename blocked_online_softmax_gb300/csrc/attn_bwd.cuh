@@ -1,6 +1,6 @@
-// Attention backward for GB300 (sm_103a). Included once, from attn_fwd_sm103.cu,
-// after the shared pieces (bounded waits, tensor maps); it is not a header for
-// other files.
+// Attention backward for GB300 (sm_103a). Included once, at the end of
+// attn_fwd_sm103.cu, after the shared pieces (bounded waits, tensor maps, the
+// host-side map encoder); it is not a header for other files.
 //
 // The method is Kernel 5 "FlashAttention Backward" of "4.4 Writing GPU Kernels
 // with Triton" (llm-stack-book): a preprocessing pass D_i = rowsum(dO_i * O_i),
@@ -10,70 +10,97 @@
 //     dV_j += P^T dO_i,   dP = dO_i V_j^T,   dS = P * (dP - D_i) * scale,
 //     dK_j += dS^T Q_i,   dQ_i += dS K_j   (scattered with fp32 atomic adds),
 // accumulating dK_j and dV_j privately and casting the fp32 dQ buffer to bf16
-// at the end.
+// at the end. An optional gradient g on the LSE output enters as D_i - g_i
+// (the derivative of LSE_i in S_ij is P_ij).
 //
-// GB300 design: one CTA per key block (192 threads): warps 0-3 compute P and
-// dS (thread = key = tensor-memory lane), warp 4 loads with TMA, warp 5 issues
-// the tcgen05 MMAs from one thread into one 512-column allocation:
-//   T0 (cols 0-127)   : S^T = K Q_i^T (fp32), then P^T as bf16 pairs over its
-//                       first 64 columns, then the dQ part dS K_j (fp32, d cols)
-//   T1 (cols 128-255) : dP^T = V dO_i^T (fp32), then dS^T as bf16 pairs
-//   T2 (cols 256-383) : dV_j (fp32, d cols)
-//   T3 (cols 384-511) : dK_j (fp32, d cols)
-// Working with the transposes keeps the key on the lane, so dV += P^T dO and
-// dK += dS^T Q take P^T and dS^T straight from tensor memory (TS MMAs); dQ =
-// dS K needs dS with the query on the lane, so the compute warps also write dS
-// to shared memory as [query][key] (K-major, 128-byte swizzle, the layout the
-// forward's shared-memory P uses), one 16-bit element per (query, own key).
-// Each block's steps run in sequence (no overlap between query blocks beyond
-// the TMA loads).
+// GB300 design: one CTA (352 threads) per (key block j of 128 keys, batch*head),
+// looping over the query blocks i of 128 queries that can see block j.
+// Measured on this GPU (microbenchmark): one thread issuing 128 x N x 16 bf16
+// MMAs into one tensor-memory allocation completes one every ~134 cycles for
+// any N up to 128, and only two threads issuing into two separate allocations
+// overlap. The five products of a block are therefore split over two issuing
+// warps, each with its own 256-column allocation:
+//   X (warp 9):  S^T = K Q_i^T into X[0,128); P^T comes back over its first
+//                64 columns as bf16 pairs; dV_j += P^T dO_i into X[128,128+d).
+//   Y (warp 10): dP^T = V dO_i^T into Y[0,128); dS^T comes back over its first
+//                64 columns; dK_j += dS^T Q_i into Y[128,128+d); then
+//                dQ_i = dS K_j (fp32) into Y[0,128) for d = 128 (after dK has
+//                read dS^T, in issue order) or into Y[192,256) for d = 64.
+// Working with the transposes keeps the key on the tensor-memory lane, so the
+// dV and dK products take P^T and dS^T straight from tensor memory.
+// Warps 0-3 (thread = key = lane) form P = exp2(S c - L2) as soon as S^T lands
+// (X can then start dV and the next block's S^T), then dS = P (dP scale -
+// D scale) once dP^T lands; dS also goes to shared memory as [query][key]
+// (128-byte swizzle, K-major), the A operand of the dQ product.
+// Warps 4-7 (thread = query = lane) take dQ_i out of tensor memory and add it
+// into the fp32 accumulation buffer with vector atomics, and stage each block's
+// LSE (base 2) and D (times scale) in shared memory two blocks ahead.
+// Warp 8 issues the TMA loads: K_j and V_j once, Q_i and dO_i into two stages.
 
 namespace bos {
 namespace {
 
 namespace bwd {
 
-constexpr int kThreads = 192;
-constexpr int kWarpProducer = 4;
-constexpr int kWarpMma = 5;
-constexpr uint32_t kT0 = 0, kT1 = 128, kT2 = 256, kT3 = 384;
+constexpr int kThreads = 352;
+constexpr int kWarpDq = 4;          // warps 4-7
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMmaX = 9;        // also allocates both tensor-memory regions
+constexpr int kWarpMmaY = 10;
+constexpr uint32_t kCols = 256;     // columns of each allocation
+constexpr uint32_t kAcc = 128;      // dV (in X) and dK (in Y) start at this column
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSmem = 232448;    // 227 KB per CTA
 
 enum : int {
     kBarKV = 0,        // K_j and V_j have landed
-    kBarQFull = 1,     // Q_i and dO_i have landed
-    kBarQFree = 2,     // every MMA of block i is complete: Q_i, dO_i and the dS buffer are free (commit)
-    kBarSFull = 3,     // S^T and dP^T of block i are complete (commit)
-    kBarPReady = 4,    // P^T and dS^T of block i are written (128 arrivals)
-    kBarDqReady = 5,   // the dQ part of block i is in T0 (commit; also covers dK, dV of block i)
-    kBarDqRead = 6,    // the dQ part has been read out of T0 (128 arrivals)
-    kBarLse = 7,       // LSE and D of block i are in shared memory (128 arrivals)
-    kBarDrain = 8,
-    kNumBars = 9,
+    kBarQFull = 1,     // [2] Q_i and dO_i of a stage have landed
+    kBarQEmpty = 3,    // [2] a stage is free: X's dV and Y's dK of its block are complete (2 commits)
+    kBarSFull = 5,     // S^T of the block is complete (X commit)
+    kBarPReady = 6,    // P^T is written (128 arrivals)
+    kBarDpFull = 7,    // dP^T of the block is complete (Y commit)
+    kBarDsReady = 8,   // dS^T (tensor memory) and dS (shared memory) are written (128 arrivals)
+    kBarDqReady = 9,   // the block's dQ part is complete (Y commit)
+    kBarDqRead = 10,   // the dQ part has been read out of tensor memory (128 arrivals)
+    kBarLseFull = 11,  // [2] LSE and D of a block are staged (128 arrivals)
+    kBarDrainX = 13,   // every MMA of X is complete
+    kBarDrainY = 14,   // every MMA of Y is complete
+    kNumBars = 15,
 };
 
 template <int D>
 struct Cfg {
     static constexpr int kTile = 128 * D * 2;                  // one bf16 128-row tile
     static constexpr int kBoxes = D / 64;
-    static constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 3 * kTile;
-    static constexpr int kOffDS = 4 * kTile;                   // dS, [128 queries][128 keys] bf16: 32 KB
-    static constexpr int kOffLse = kOffDS + 32768;             // [2][128] LSE * log2 e, then [2][128] D
-    static constexpr int kOffBar = kOffLse + 2 * 2 * 128 * 4;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr int kOffK = 0, kOffV = kTile;
+    static constexpr int kOffStage = 2 * kTile;                // stage s: Q_i, then dO_i
+    static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kOffDS = 6 * kTile;                   // dS, [128 queries][128 keys] bf16: 32 KB
+    static constexpr int kOffLse = kOffDS + 32768;             // [2][128] LSE * log2 e, then [2][128] D * scale
+    static constexpr int kOffBar = kOffLse + 2048;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // two tensor-memory slots, abort flag
+    static constexpr int kUsed = kOffMisc + 16;
+    // 1 KB to align the tiles by hand when it fits; otherwise the kernel checks
+    // that the dynamic shared memory it was given starts 1024-byte aligned
+    static constexpr int kPad = (kUsed + 1024 <= kMaxSmem) ? 1024 : 0;
+    static constexpr int kSmemBytes = kUsed + kPad;
+    static constexpr uint32_t kTdQ = (D == 64) ? 192u : 0u;    // dQ columns in Y
+    static_assert(kSmemBytes <= kMaxSmem, "shared memory over the per-CTA limit");
 };
 
 struct BwdArgs {
     int BH, N, d, nkv, causal;
     float scale, c2;                  // c2 = scale * log2 e
     const float* lse;                 // [BH, N] natural log, from the forward pass
-    const float* dsum;                // [BH, N] D = rowsum(dO * O)
+    const float* dsum;                // [BH, N] D = rowsum(dO * O) - dLSE
     float* dq_acc;                    // [BH, N, d] fp32, zeroed before the launch
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     uint64_t wait_limit_ns;
 };
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
@@ -85,133 +112,194 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         tma_load_3d(smem + C::kOffK + b * 16384, tm_k, &bars[kBarKV], b * 64, j * 128, bh);
         tma_load_3d(smem + C::kOffV + b * 16384, tm_v, &bars[kBarKV], b * 64, j * 128, bh);
     }
-    int last = -1;
+    int last[2] = {-1, -1};
     for (int it = 0; it < nq; ++it) {
-        const int i = i0 + it;
-        // Q_i and dO_i reuse one buffer: wait until block it-1's MMAs are done with it
-        if (it > 0 && !wait_or_abort(&bars[kBarQFree], (uint32_t)((it - 1) & 1), a.wait_limit_ns, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * C::kTile);
+        const int s = it & 1;
+        // the stage's previous block (it - 2) must be released by both issuers
+        if (it >= 2 && !wait_or_abort(&bars[kBarQEmpty + s], (uint32_t)(((it >> 1) + 1) & 1), a.wait_limit_ns,
+                                      abort_flag))
+            break;
+        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&bars[kBarQFull + s], 2 * C::kTile);
         for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(smem + C::kOffQ + b * 16384, tm_q, &bars[kBarQFull], b * 64, i * 128, bh);
-            tma_load_3d(smem + C::kOffDO + b * 16384, tm_do, &bars[kBarQFull], b * 64, i * 128, bh);
+            tma_load_3d(st + b * 16384, tm_q, &bars[kBarQFull + s], b * 64, (i0 + it) * 128, bh);
+            tma_load_3d(st + C::kTile + b * 16384, tm_do, &bars[kBarQFull + s], b * 64, (i0 + it) * 128, bh);
         }
-        last = it;
+        last[s] = it;
     }
     // every copy this thread started must land before the CTA may exit
     mbar_wait(&bars[kBarKV], 0, kDrainLimitNs);
-    if (last >= 0) mbar_wait(&bars[kBarQFull], (uint32_t)(last & 1), kDrainLimitNs);
+    for (int s = 0; s < 2; ++s)
+        if (last[s] >= 0) mbar_wait(&bars[kBarQFull + s], (uint32_t)((last[s] >> 1) & 1), kDrainLimitNs);
 }
 
+// X: S^T = K Q_i^T, then dV_j += P^T dO_i once P^T is written.
 template <int D>
-__device__ void mma_issuer(uint32_t tm, uint8_t* smem, uint64_t* bars, volatile int* abort_flag, int nq,
-                           const BwdArgs& a) {
+__device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* abort_flag, int nq,
+                      const BwdArgs& a) {
     using C = Cfg<D>;
     const uint64_t lim = a.wait_limit_ns;
-    const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
-    const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
-    const uint32_t sDS = smem_u32(smem + C::kOffDS);
-    // S^T, dP^T: M = 128 keys, N = 128 queries, K = d, both operands K-major
+    const uint32_t sK = smem_u32(smem + C::kOffK);
+    // M = 128 keys, N = 128 queries, K = d; both operands K-major
     constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-    // dV, dK: M = 128 keys, N = d, K = 128 queries; A from tensor memory, B (dO, Q) N-major
+    // M = 128 keys, N = d, K = 128 queries; A from tensor memory, B (dO) N-major
     constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
-    // dQ: M = 128 queries, N = d, K = 128 keys; A (dS in shared memory) K-major, B (K_j) N-major
+    bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
+    for (int it = 0; ok && it < nq; ++it) {
+        const int s = it & 1;
+        const uint32_t sQ = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        const uint32_t sDO = sQ + C::kTile;
+        if (!wait_or_abort(&bars[kBarQFull + s], (uint32_t)((it >> 1) & 1), lim, abort_flag)) break;
+        tc_fence_after();
+        // overwrites P^T of the previous block, which that block's dV (issued earlier) reads
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+            mma_ss(tX, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[kBarSFull]);
+        if (!wait_or_abort(&bars[kBarPReady], (uint32_t)(it & 1), lim, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // 16 queries per step: 8 columns of bf16 pairs, 16 rows of dO
+            mma_ts(tX + kAcc, tX + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), id_kv,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarQEmpty + s]);
+    }
+    mma_commit(&bars[kBarDrainX]);
+    mbar_wait(&bars[kBarDrainX], 0, kDrainLimitNs);
+}
+
+// Y: dP^T = V dO_i^T, then dK_j += dS^T Q_i and dQ_i = dS K_j once dS is written.
+template <int D>
+__device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* abort_flag, int nq,
+                      const BwdArgs& a) {
+    using C = Cfg<D>;
+    constexpr bool kDqOverDp = (C::kTdQ == 0);   // dQ reuses the dP^T columns
+    const uint64_t lim = a.wait_limit_ns;
+    const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
+    const uint32_t sDS = smem_u32(smem + C::kOffDS);
+    constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+    // M = 128 queries, N = d, K = 128 keys; A (dS) K-major, B (K_j) N-major
     constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);
     bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
     for (int it = 0; ok && it < nq; ++it) {
-        const uint32_t par = (uint32_t)(it & 1);
-        if (!wait_or_abort(&bars[kBarQFull], par, lim, abort_flag)) break;
-        // T0 is free once the compute warps have read the previous dQ part
-        if (it > 0 && !wait_or_abort(&bars[kBarDqRead], par ^ 1, lim, abort_flag)) break;
+        const int s = it & 1;
+        const uint32_t sQ = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        const uint32_t sDO = sQ + C::kTile;
+        if (!wait_or_abort(&bars[kBarQFull + s], (uint32_t)((it >> 1) & 1), lim, abort_flag)) break;
+        if (kDqOverDp && it > 0 && !wait_or_abort(&bars[kBarDqRead], (uint32_t)((it - 1) & 1), lim, abort_flag))
+            break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-            mma_ss(tm + kT0, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+            mma_ss(tY, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-            mma_ss(tm + kT1, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars[kBarSFull]);
-        if (!wait_or_abort(&bars[kBarPReady], par, lim, abort_flag)) break;
+        mma_commit(&bars[kBarDpFull]);
+        if (!wait_or_abort(&bars[kBarDsReady], (uint32_t)(it & 1), lim, abort_flag)) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)   // 16 queries per step: 8 columns of bf16 pairs, 16 rows of dO / Q
-            mma_ts(tm + kT2, tm + kT0 + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), id_kv,
-                   (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tm + kT3, tm + kT1 + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv,
+            mma_ts(tY + kAcc, tY + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv,
                    (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarQEmpty + s]);
+        if (!kDqOverDp && it > 0 && !wait_or_abort(&bars[kBarDqRead], (uint32_t)((it - 1) & 1), lim, abort_flag))
+            break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // 16 keys per step: 32 bytes of each dS row, 16 rows of K_j
-            mma_ss(tm + kT0, sdesc_sw128(sDS + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+            mma_ss(tY + C::kTdQ, sdesc_sw128(sDS + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
                    sdesc_sw128(sK + kk * 2048, 16384, 1024), id_q, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarDqReady]);
-        mma_commit(&bars[kBarQFree]);
     }
-    mma_commit(&bars[kBarDrain]);
-    mbar_wait(&bars[kBarDrain], 0, kDrainLimitNs);
+    mma_commit(&bars[kBarDrainY]);
+    mbar_wait(&bars[kBarDrainY], 0, kDrainLimitNs);
+}
+
+// P^T of one block into tensor memory (over the S^T columns already read) and
+// into registers as bf16 pairs (queries 2e, 2e+1 of each 32-query chunk).
+template <bool kMasked>
+__device__ __forceinline__ void p_phase(uint32_t lx, const float* L, float c2, int r, bool key_ok, bool diag,
+                                        uint32_t (&pk)[64]) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32];
+        tmem_ld32(lx + ch * 32, sv);
+        uint32_t t[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int qc = ch * 32 + 2 * e;
+            const float2 l2 = *reinterpret_cast<const float2*>(L + qc);
+            float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, -l2.x));
+            float p1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -l2.y));
+            if (kMasked) {
+                if (!key_ok || (diag && qc < r)) p0 = 0.f;
+                if (!key_ok || (diag && qc + 1 < r)) p1 = 0.f;
+            }
+            t[e] = pack_bf16(p0, p1);
+            pk[ch * 16 + e] = t[e];
+        }
+        tmem_st16(lx + ch * 16, t);
+    }
 }
 
 template <int D>
-__device__ void compute_role(uint32_t tm, int w, int lane, uint8_t* smem, uint64_t* bars, volatile int* abort_flag,
-                             int bh, int j, int i0, int nq, const BwdArgs& a) {
+__device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* bars,
+                             volatile int* abort_flag, int bh, int j, int nq, const BwdArgs& a) {
     using C = Cfg<D>;
     const uint64_t lim = a.wait_limit_ns;
-    const int r = w * 32 + lane;                              // tensor-memory lane
-    const uint32_t lane_base = tm + ((uint32_t)(w * 32) << 16);
-    float* lse_s = reinterpret_cast<float*>(smem + C::kOffLse);         // [2][128]
-    float* d_s = lse_s + 2 * 128;                                        // [2][128]
+    const int r = w * 32 + lane;                              // tensor-memory lane = key within the block
+    const uint32_t lx = tX + ((uint32_t)(w * 32) << 16), ly = tY + ((uint32_t)(w * 32) << 16);
+    const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffLse);   // [2][128]
+    const float* dsc_s = lse_s + 2 * 128;                                      // [2][128]
     // this thread's key in the [query][key] dS buffer: box r / 64, 16-byte chunk
     // (r % 64) / 8 (swizzled with the query row), element r % 8
     uint8_t* ds_col = smem + C::kOffDS + (r >> 6) * 16384 + (r & 7) * 2;
     const int ds_chunk = (r & 63) >> 3;
     const int key = j * 128 + r;
+    const bool key_ok = key < a.N;
+    const bool tail_block = j * 128 + 128 > a.N;
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
         bool got = wait_or_abort(bar, parity, lim, abort_flag);
         return __all_sync(0xffffffffu, got);
     };
-    bool ok = true;
     for (int it = 0; it < nq; ++it) {
         const uint32_t par = (uint32_t)(it & 1);
-        const int q0 = (i0 + it) * 128;
-        // this block's LSE (to base 2) and D, one query per thread, into shared memory
-        {
-            const int q = q0 + r;
-            const int b = it & 1;
-            lse_s[b * 128 + r] = (q < a.N) ? a.lse[(int64_t)bh * a.N + q] * kLog2e : INFINITY;
-            d_s[b * 128 + r] = (q < a.N) ? a.dsum[(int64_t)bh * a.N + q] : 0.f;
-            mbar_arrive(&bars[kBarLse]);
-        }
-        if (!wait_warp(&bars[kBarLse], par) || !wait_warp(&bars[kBarSFull], par)) { ok = false; break; }
+        const int lb = it & 1;
+        if (!wait_warp(&bars[kBarLseFull + lb], (uint32_t)((it >> 1) & 1)) || !wait_warp(&bars[kBarSFull], par))
+            return;
         tc_fence_after();
-        const float* lse_b = lse_s + (it & 1) * 128;
-        const float* d_b = d_s + (it & 1) * 128;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {                      // 32 queries per chunk
-            uint32_t sv[32], dpv[32];
-            tmem_ld32(lane_base + kT0 + ch * 32, sv);
-            tmem_ld32(lane_base + kT1 + ch * 32, dpv);
-            uint32_t pk[16], dk[16];
+        const float* L = lse_s + lb * 128;
+        const float* Dsc = dsc_s + lb * 128;
+        const bool diag = a.causal && it == 0;               // the first query block is block j itself
+        uint32_t pk[64];
+        if (diag || tail_block)
+            p_phase<true>(lx, L, a.c2, r, key_ok, diag, pk);
+        else
+            p_phase<false>(lx, L, a.c2, r, key_ok, diag, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kBarPReady]);
+
+        if (!wait_warp(&bars[kBarDpFull], par)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t dpv[32];
+            tmem_ld32(ly + ch * 32, dpv);
+            uint32_t dk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                float pp[2], dd[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int qc = ch * 32 + 2 * e + h;
-                    const int q = q0 + qc;
-                    const bool valid = key < a.N && (!a.causal || q >= key);
-                    const float p = valid ? ex2(fmaf(__uint_as_float(sv[2 * e + h]), a.c2, -lse_b[qc])) : 0.f;
-                    pp[h] = p;
-                    dd[h] = p * (__uint_as_float(dpv[2 * e + h]) - d_b[qc]) * a.scale;
-                }
-                pk[e] = pack_bf16(pp[0], pp[1]);
-                dk[e] = pack_bf16(dd[0], dd[1]);
+                const int qc = ch * 32 + 2 * e;
+                const float2 dd = *reinterpret_cast<const float2*>(Dsc + qc);
+                const uint32_t p = pk[ch * 16 + e];
+                const float ds0 = bf16_lo(p) * fmaf(__uint_as_float(dpv[2 * e]), a.scale, -dd.x);
+                const float ds1 = bf16_hi(p) * fmaf(__uint_as_float(dpv[2 * e + 1]), a.scale, -dd.y);
+                dk[e] = pack_bf16(ds0, ds1);
             }
-            tmem_st16(lane_base + kT0 + ch * 16, pk);         // P^T over S^T columns already read
-            tmem_st16(lane_base + kT1 + ch * 16, dk);         // dS^T over dP^T columns already read
+            tmem_st16(ly + ch * 16, dk);                      // dS^T over dP^T columns already read
 #pragma unroll
             for (int e = 0; e < 32; ++e) {                    // dS[query][key r], queries 32ch..32ch+31
                 const int qr = ch * 32 + e;
@@ -223,59 +311,84 @@ __device__ void compute_role(uint32_t tm, int w, int lane, uint8_t* smem, uint64
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars[kBarPReady]);
-        // the dQ part: lane r is now query q0 + r
-        if (!wait_warp(&bars[kBarDqReady], par)) { ok = false; break; }
-        tc_fence_after();
-        {
-            const int q = q0 + r;
-            float* dst = a.dq_acc + ((int64_t)bh * a.N + q) * a.d;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + kT0 + c0, v);
-                if (q < a.N) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        if (c0 + e < a.d)
-                            atomicAdd(reinterpret_cast<float4*>(dst + c0 + e),
-                                      make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                                  __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
-                }
-            }
-        }
-        tc_fence_before();
-        mbar_arrive(&bars[kBarDqRead]);
+        mbar_arrive(&bars[kBarDsReady]);
     }
-    if (!ok) return;
-    // dK_j and dV_j are final once the last block's dQ part was ready (same commit).
+    // dV_j is final once all of X's MMAs are complete, dK_j once all of Y's are.
     // The tensor-memory loads are warp-collective: every lane takes part, and
     // only the stores depend on the lane's key being inside the sequence.
-    tc_fence_after();
-    {
-        __nv_bfloat16* dkr = a.dk + ((int64_t)bh * a.N + key) * a.d;
-        __nv_bfloat16* dvr = a.dv + ((int64_t)bh * a.N + key) * a.d;
+    __nv_bfloat16* dkr = a.dk + ((int64_t)bh * a.N + key) * a.d;
+    __nv_bfloat16* dvr = a.dv + ((int64_t)bh * a.N + key) * a.d;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        if (!wait_warp(&bars[pass == 0 ? kBarDrainX : kBarDrainY], 0)) return;
+        tc_fence_after();
+        const uint32_t src = (pass == 0 ? lx : ly) + kAcc;
+        __nv_bfloat16* dst = pass == 0 ? dvr : dkr;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t kv[32], vv[32];
-            tmem_ld32(lane_base + kT3 + c0, kv);
-            tmem_ld32(lane_base + kT2 + c0, vv);
-            if (key >= a.N) continue;
+            uint32_t v[32];
+            tmem_ld32(src + c0, v);
+            if (!key_ok) continue;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
                 if (c0 + e >= a.d) break;
-                uint4 wk, wv;
-                wk.x = pack_bf16(__uint_as_float(kv[e]), __uint_as_float(kv[e + 1]));
-                wk.y = pack_bf16(__uint_as_float(kv[e + 2]), __uint_as_float(kv[e + 3]));
-                wk.z = pack_bf16(__uint_as_float(kv[e + 4]), __uint_as_float(kv[e + 5]));
-                wk.w = pack_bf16(__uint_as_float(kv[e + 6]), __uint_as_float(kv[e + 7]));
-                wv.x = pack_bf16(__uint_as_float(vv[e]), __uint_as_float(vv[e + 1]));
-                wv.y = pack_bf16(__uint_as_float(vv[e + 2]), __uint_as_float(vv[e + 3]));
-                wv.z = pack_bf16(__uint_as_float(vv[e + 4]), __uint_as_float(vv[e + 5]));
-                wv.w = pack_bf16(__uint_as_float(vv[e + 6]), __uint_as_float(vv[e + 7]));
-                *reinterpret_cast<uint4*>(dkr + c0 + e) = wk;
-                *reinterpret_cast<uint4*>(dvr + c0 + e) = wv;
+                uint4 wv;
+                wv.x = pack_bf16(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                wv.y = pack_bf16(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                wv.z = pack_bf16(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+                wv.w = pack_bf16(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+                *reinterpret_cast<uint4*>(dst + c0 + e) = wv;
             }
+        }
+    }
+}
+
+// Warps 4-7: stage LSE / D two blocks ahead, read each dQ part out of tensor
+// memory (freeing its columns for Y) and add it into the fp32 buffer.
+template <int D>
+__device__ void dq_role(uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* bars, volatile int* abort_flag,
+                        int bh, int i0, int nq, const BwdArgs& a) {
+    using C = Cfg<D>;
+    const uint64_t lim = a.wait_limit_ns;
+    const int r = (w & 3) * 32 + lane;                        // tensor-memory lane = query within the block
+    const uint32_t ly = tY + ((uint32_t)((w & 3) * 32) << 16) + C::kTdQ;
+    float* lse_s = reinterpret_cast<float*>(smem + C::kOffLse);
+    float* dsc_s = lse_s + 2 * 128;
+    auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+        bool got = wait_or_abort(bar, parity, lim, abort_flag);
+        return __all_sync(0xffffffffu, got);
+    };
+    auto stage = [&](int it) {
+        const int q = (i0 + it) * 128 + r;
+        const int b = it & 1;
+        const bool in = q < a.N;
+        lse_s[b * 128 + r] = in ? a.lse[(int64_t)bh * a.N + q] * kLog2e : INFINITY;
+        dsc_s[b * 128 + r] = in ? a.dsum[(int64_t)bh * a.N + q] * a.scale : 0.f;
+        mbar_arrive(&bars[kBarLseFull + b]);
+    };
+    stage(0);
+    if (nq > 1) stage(1);
+    for (int it = 0; it < nq; ++it) {
+        if (!wait_warp(&bars[kBarDqReady], (uint32_t)(it & 1))) return;
+        tc_fence_after();
+        uint32_t v[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(ly + c * 32, v + c * 32);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld_wait32(v + c * 32);
+        tc_fence_before();
+        mbar_arrive(&bars[kBarDqRead]);
+        // the compute warps finished with this buffer before Y could form this dQ part
+        if (it + 2 < nq) stage(it + 2);
+        const int q = (i0 + it) * 128 + r;
+        if (q < a.N) {
+            float* dst = a.dq_acc + ((int64_t)bh * a.N + q) * a.d;
+#pragma unroll
+            for (int e = 0; e < D; e += 4)
+                if (e < a.d)
+                    atomicAdd(reinterpret_cast<float4*>(dst + e),
+                              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
         }
     }
 }
@@ -289,8 +402,15 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const bwd::BwdArgs a) {
     using C = bwd::Cfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw;
+    if (C::kPad) {
+        smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    } else if (smem_u32(smem_raw) & 1023u) {
+        // the swizzled tiles need 1024-byte alignment and there is no room to pad
+        if (threadIdx.x == 0) atomicCAS(&g_attn_device_status, 0, (int)ATTN_ERR_LAUNCH);
+        return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
@@ -301,14 +421,19 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[bwd::kBarKV], 1);
-        mbar_init(&bars[bwd::kBarQFull], 1);
-        mbar_init(&bars[bwd::kBarQFree], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[bwd::kBarQFull + s], 1);
+            mbar_init(&bars[bwd::kBarQEmpty + s], 2);
+            mbar_init(&bars[bwd::kBarLseFull + s], 128);
+        }
         mbar_init(&bars[bwd::kBarSFull], 1);
         mbar_init(&bars[bwd::kBarPReady], 128);
+        mbar_init(&bars[bwd::kBarDpFull], 1);
+        mbar_init(&bars[bwd::kBarDsReady], 128);
         mbar_init(&bars[bwd::kBarDqReady], 1);
         mbar_init(&bars[bwd::kBarDqRead], 128);
-        mbar_init(&bars[bwd::kBarLse], 128);
-        mbar_init(&bars[bwd::kBarDrain], 1);
+        mbar_init(&bars[bwd::kBarDrainX], 1);
+        mbar_init(&bars[bwd::kBarDrainY], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -318,56 +443,149 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
     }
-    if (warp == bwd::kWarpMma) {
-        tmem_alloc(tmem_slot, 512);
+    if (warp == bwd::kWarpMmaX) {
+        tmem_alloc(tmem_slot, bwd::kCols);
+        tmem_alloc(tmem_slot + 1, bwd::kCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tm = tmem_slot[0];
+    const uint32_t tX = tmem_slot[0], tY = tmem_slot[1];
 
-    if (warp < 4) {
-        bwd::compute_role<D>(tm, warp, lane, smem, bars, abort_flag, bh, j, i0, nq, a);
+    if (warp < bwd::kWarpDq) {
+        bwd::compute_role<D>(tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
+    } else if (warp < bwd::kWarpProducer) {
+        bwd::dq_role<D>(tY, warp, lane, smem, bars, abort_flag, bh, i0, nq, a);
     } else if (warp == bwd::kWarpProducer) {
         if (lane == 0) bwd::producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, smem, bars, abort_flag, bh, j, i0, nq, a);
         __syncwarp();
+    } else if (warp == bwd::kWarpMmaX) {
+        if (lane == 0) bwd::mma_x<D>(tX, smem, bars, abort_flag, nq, a);
+        __syncwarp();
     } else {
-        if (lane == 0) bwd::mma_issuer<D>(tm, smem, bars, abort_flag, nq, a);
+        if (lane == 0) bwd::mma_y<D>(tY, smem, bars, abort_flag, nq, a);
         __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == bwd::kWarpMma) tmem_dealloc(tm, 512);
-}
-
-// D = rowsum(dO * O) in fp32 per row, and the fp32 dQ buffer zeroed: one warp per row.
-__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                                                           const __nv_bfloat16* __restrict__ dout,
-                                                           float* __restrict__ dsum, float* __restrict__ dq_acc,
-                                                           int64_t rows, int d) {
-    const int lane = threadIdx.x % 32;
-    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; row < rows;
-         row += (int64_t)gridDim.x * blockDim.x / 32) {
-        const __nv_bfloat16* orow = o + row * d;
-        const __nv_bfloat16* grow = dout + row * d;
-        float s = 0.f;
-        for (int c = lane; c < d; c += 32) s += __bfloat162float(orow[c]) * __bfloat162float(grow[c]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) dsum[row] = s;
-        for (int c = lane; c < d; c += 32) dq_acc[row * d + c] = 0.f;
+    if (warp == bwd::kWarpMmaX) {
+        tmem_dealloc(tX, bwd::kCols);
+        tmem_dealloc(tY, bwd::kCols);
     }
 }
 
-// dQ: the fp32 accumulation buffer to bf16.
+// D = rowsum(dO * O) - dLSE in fp32 per row, and the fp32 dQ buffer zeroed. One
+// warp per row; lane l covers columns 8l..8l+7 (d is a multiple of 8 up to 128).
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                           const __nv_bfloat16* __restrict__ dout,
+                                                           const float* __restrict__ dlse,
+                                                           float* __restrict__ dsum, float* __restrict__ dq_acc,
+                                                           int64_t rows, int d) {
+    const int lane = threadIdx.x % 32;
+    const int c = lane * 8;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; row < rows;
+         row += (int64_t)gridDim.x * blockDim.x / 32) {
+        float s = 0.f;
+        if (c < d) {
+            const uint4 ov = *reinterpret_cast<const uint4*>(o + row * d + c);
+            const uint4 gv = *reinterpret_cast<const uint4*>(dout + row * d + c);
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                s += bwd::bf16_lo(ow[e]) * bwd::bf16_lo(gw[e]) + bwd::bf16_hi(ow[e]) * bwd::bf16_hi(gw[e]);
+            float4* z = reinterpret_cast<float4*>(dq_acc + row * d + c);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) dsum[row] = dlse ? s - dlse[row] : s;
+    }
+}
+
+// dQ: the fp32 accumulation buffer to bf16, eight values per thread (n % 8 == 0).
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restrict__ dq_acc,
-                                                            __nv_bfloat16* __restrict__ dq, int64_t n) {
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x)
-        dq[idx] = __float2bfloat16_rn(dq_acc[idx]);
+                                                            __nv_bfloat16* __restrict__ dq, int64_t n8) {
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
+        const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
+        uint4 w;
+        w.x = pack_bf16(a.x, a.y);
+        w.y = pack_bf16(a.z, a.w);
+        w.z = pack_bf16(b.x, b.y);
+        w.w = pack_bf16(b.z, b.w);
+        reinterpret_cast<uint4*>(dq)[idx] = w;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int D>
+int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
+    using C = bwd::Cfg<D>;
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return ATTN_ERR_CUDA;
+    const int BH = p.B * p.H;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, p.d, 128) ||
+        !encode_qkv_map(enc, &mv, p.v, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mdo, p.dout, BH, p.N, p.d, 128))
+        return ATTN_ERR_BAD_SHAPE;
+    static int attr_done[64] = {0};
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        if (cudaFuncSetAttribute(attn_bwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_LAUNCH;
+        }
+        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+    }
+    const int64_t rows = (int64_t)BH * p.N;
+    float* dq_acc = static_cast<float*>(p.workspace);
+    const size_t acc_bytes = ((size_t)rows * p.d * sizeof(float) + 255) & ~(size_t)255;
+    float* dsum = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + acc_bytes);
+    const int64_t pre_blocks = (rows + 7) / 8;   // 8 rows (warps) per 256-thread block
+    attn_bwd_pre_kernel<<<(unsigned)(pre_blocks < 1048576 ? pre_blocks : 1048576), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.dlse, dsum, dq_acc, rows,
+        p.d);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    bwd::BwdArgs a;
+    a.BH = BH;
+    a.N = p.N;
+    a.d = p.d;
+    a.nkv = (p.N + 127) / 128;
+    a.causal = p.causal;
+    a.scale = p.scale;
+    a.c2 = (float)((double)p.scale * 1.4426950408889634);
+    a.lse = p.lse;
+    a.dsum = dsum;
+    a.dq_acc = dq_acc;
+    a.dk = static_cast<__nv_bfloat16*>(p.dk);
+    a.dv = static_cast<__nv_bfloat16*>(p.dv);
+    a.wait_limit_ns = g_wait_limit_ns;
+    const int64_t grid = (int64_t)BH * a.nkv;
+    attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    const int64_t n8 = rows * p.d / 8;
+    const int64_t post_blocks = (n8 + 255) / 256;
+    attn_bwd_post_kernel<<<(unsigned)(post_blocks < 1048576 ? post_blocks : 1048576), 256, 0, stream>>>(
+        dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 }  // namespace
+
+size_t attn_bwd_workspace(int B, int H, int N, int d) {
+    const size_t rows = (size_t)B * H * N;
+    const size_t acc = (rows * d * sizeof(float) + 255) & ~(size_t)255;
+    return acc + ((rows * sizeof(float) + 255) & ~(size_t)255);
+}
+
+int launch_attn_bwd(const AttnBwdParams& p, cudaStream_t stream, int dev) {
+    return p.d <= 64 ? launch_bwd_d<64>(p, stream, dev) : launch_bwd_d<128>(p, stream, dev);
+}
+
 }  // namespace bos

@@ -803,7 +803,6 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 }  // namespace bos
 
 #include "attn_fwd_d64.cuh"
-#include "attn_bwd.cuh"
 
 namespace bos {
 namespace {
@@ -921,71 +920,6 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
 
 }  // namespace
 
-size_t attn_bwd_workspace(int B, int H, int N, int d) {
-    const size_t rows = (size_t)B * H * N;
-    const size_t acc = (rows * d * sizeof(float) + 255) & ~(size_t)255;
-    return acc + ((rows * sizeof(float) + 255) & ~(size_t)255);
-}
-
-namespace {
-
-template <int D>
-int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
-    using C = bwd::Cfg<D>;
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc) return ATTN_ERR_CUDA;
-    const int BH = p.B * p.H;
-    CUtensorMap mq, mk, mv, mdo;
-    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, p.d, 128) ||
-        !encode_qkv_map(enc, &mv, p.v, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mdo, p.dout, BH, p.N, p.d, 128))
-        return ATTN_ERR_BAD_SHAPE;
-    static int attr_done[64] = {0};
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        if (cudaFuncSetAttribute(attn_bwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess) {
-            cudaGetLastError();
-            return ATTN_ERR_LAUNCH;
-        }
-        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
-    }
-    const int64_t rows = (int64_t)BH * p.N;
-    float* dq_acc = static_cast<float*>(p.workspace);
-    const size_t acc_bytes = ((size_t)rows * p.d * sizeof(float) + 255) & ~(size_t)255;
-    float* dsum = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + acc_bytes);
-    const int64_t pre_blocks = (rows + 7) / 8;   // 8 rows (warps) per 256-thread block
-    attn_bwd_pre_kernel<<<(unsigned)(pre_blocks < 1048576 ? pre_blocks : 1048576), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), dsum, dq_acc, rows, p.d);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-    bwd::BwdArgs a;
-    a.BH = BH;
-    a.N = p.N;
-    a.d = p.d;
-    a.nkv = (p.N + 127) / 128;
-    a.causal = p.causal;
-    a.scale = p.scale;
-    a.c2 = (float)((double)p.scale * 1.4426950408889634);
-    a.lse = p.lse;
-    a.dsum = dsum;
-    a.dq_acc = dq_acc;
-    a.dk = static_cast<__nv_bfloat16*>(p.dk);
-    a.dv = static_cast<__nv_bfloat16*>(p.dv);
-    a.wait_limit_ns = g_wait_limit_ns;
-    const int64_t grid = (int64_t)BH * a.nkv;
-    attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-    const int64_t n = rows * p.d;
-    const int64_t post_blocks = (n + 255) / 256;
-    attn_bwd_post_kernel<<<(unsigned)(post_blocks < 1048576 ? post_blocks : 1048576), 256, 0, stream>>>(
-        dq_acc, static_cast<__nv_bfloat16*>(p.dq), n);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
-}
-
-}  // namespace
-
-int launch_attn_bwd(const AttnBwdParams& p, cudaStream_t stream, int dev) {
-    return p.d <= 64 ? launch_bwd_d<64>(p, stream, dev) : launch_bwd_d<128>(p, stream, dev);
-}
-
 int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev) {
     // head dims below a kernel's width run on it with the missing columns
     // zero-filled by TMA on load and clipped on store
@@ -1011,3 +945,5 @@ int read_and_clear_device_status(cudaStream_t stream) {
 }
 
 }  // namespace bos
+
+#include "attn_bwd.cuh"

@@ -46,6 +46,7 @@ struct AttnBwdParams {
     const void* o;
     const void* dout;
     const float* lse;
+    const float* dlse;   // optional gradient on lse (may be null)
     void* dq;
     void* dk;
     void* dv;

@@ -167,10 +167,15 @@ int attn_abi_version(void);
  *
  *     dq = dS k,   dk = dS^T q,   dv = P^T dO.
  *
+ * A gradient g on the LSE output (dL/dLSE) may be passed as dlse; since the
+ * derivative of LSE_i in the score S_ij is P_ij, it enters as D_i - g_i.
+ *
  *   q, k, v, o, dout : bf16, contiguous [B, H, N, d], device memory, 16-byte
  *                      aligned; o and lse are attn_fwd's outputs for the same
  *                      q, k, v, scale and causal; dout is dL/dO.
  *   lse              : fp32 [B, H, N], device memory, 4-byte aligned.
+ *   dlse             : fp32 [B, H, N] gradient on lse, device memory, 4-byte
+ *                      aligned; NULL when the loss does not depend on lse.
  *   dq, dk, dv       : bf16 [B, H, N, d] outputs, 16-byte aligned.
  *   workspace        : device memory of workspace_bytes >=
  *                      attn_bwd_workspace_bytes(B, H, N, d), 256-byte aligned:
@@ -184,7 +189,7 @@ int attn_abi_version(void);
  * nothing is launched or written.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+             const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
              float scale, int causal, void* stream);
 
 /* Workspace bytes attn_bwd needs for these sizes (0 if B, H, N or d are out of range). */

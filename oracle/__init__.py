@@ -125,7 +125,7 @@ def softmax_row(x):
     return p, float(lse)
 
 
-def attention_bwd(q, k, v, do, scale: float, causal: bool):
+def attention_bwd(q, k, v, do, scale: float, causal: bool, dlse=None):
     """dq, dk, dv in fp64 for inputs shaped [B,H,N,d] (bf16 tensors or float arrays) and dO.
 
     The definition the backward pass computes ("4.4 Writing GPU Kernels with
@@ -133,9 +133,14 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool):
     score matrix materialised: S = scale q k^T (causal: -inf above the
     diagonal), P = softmax(S) by rows, O = P v, dv = P^T dO, dP = dO v^T,
     D = rowsum(dO * O), dS = P * (dP - D), dq = scale dS k, dk = scale dS^T q.
+
+    ``dlse`` ([B,H,N], optional) is a gradient on the forward's second output,
+    LSE_i = log sum_j exp(S_ij). Its derivative in S_ij is P_ij, so it enters
+    as dS = P * (dP - D + dlse), i.e. D is replaced by D - dlse.
     """
     qa, ka, va, ga = (_to_f64(t) for t in (q, k, v, do))
     B, H, N, d = qa.shape
+    gl = None if dlse is None else _to_f64(dlse).reshape(B, H, N)
     dq = np.zeros_like(qa)
     dk = np.zeros_like(ka)
     dv = np.zeros_like(va)
@@ -152,6 +157,8 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool):
             dv[b, h] = P.T @ G
             dP = G @ V.T
             Dr = (G * O).sum(axis=1, keepdims=True)
+            if gl is not None:
+                Dr = Dr - gl[b, h][:, None]
             dS = P * (dP - Dr)
             dq[b, h] = scale * (dS @ K)
             dk[b, h] = scale * (dS.T @ Q)

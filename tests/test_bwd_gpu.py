@@ -29,10 +29,11 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def grads_gpu(q, k, v, g, scale, causal):
+def grads_gpu(q, k, v, g, scale, causal, dlse=None):
     B, H, N, d = q.shape
     dev = torch.device("cuda")
     qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    dl = None if dlse is None else dlse.to(dev).contiguous()
     o = torch.empty_like(qd)
     lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     bos.attn_fwd(qd, kd, vd, o, lse, B, H, N, d, scale, causal, None)
@@ -43,7 +44,7 @@ def grads_gpu(q, k, v, g, scale, causal):
         outs.append(buf)
     nbytes = bos.attn_bwd_workspace_bytes(B, H, N, d)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    bos.attn_bwd(qd, kd, vd, o, gd, lse, outs[0], outs[1], outs[2], ws, nbytes, B, H, N, d, scale, causal, None)
+    bos.attn_bwd(qd, kd, vd, o, gd, lse, dl, outs[0], outs[1], outs[2], ws, nbytes, B, H, N, d, scale, causal, None)
     torch.cuda.synchronize()
     res = []
     for buf in outs:
@@ -92,3 +93,43 @@ def test_backward_large_logits():
     gpu = grads_gpu(q, k, v, g, 0.125, True)
     ref = oracle.attention_bwd(q, k, v, g, 0.125, True)
     check(gpu, ref, "x4 logits")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_lse_gradient(d, causal):
+    """A gradient on the LSE output as well: the kernel takes D - dLSE."""
+    q, k, v = make_qkv(1, 2, 333, d, seed=80 + d)
+    g = dout_like(q, 81)
+    gl = torch.randn(1, 2, 333, generator=torch.Generator().manual_seed(82), dtype=torch.float32)
+    scale = float(np.float32(d ** -0.5))
+    gpu = grads_gpu(q, k, v, g, scale, causal, dlse=gl)
+    ref = oracle.attention_bwd(q, k, v, g, scale, causal, dlse=gl.numpy())
+    check(gpu, ref, f"dlse d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True), (32, True), (120, False)])
+def test_backward_long(d, causal):
+    """Many query blocks per key block: both Q/dO stages and LSE buffers are reused many times."""
+    q, k, v = make_qkv(1, 1, 2000, d, seed=90 + d)
+    g = dout_like(q, 91)
+    scale = float(np.float32(d ** -0.5))
+    gpu = grads_gpu(q, k, v, g, scale, causal)
+    ref = oracle.attention_bwd(q, k, v, g, scale, causal)
+    check(gpu, ref, f"N=2000 d={d} causal={causal}")
+
+
+def test_backward_full_size_sampled_head():
+    """The 8K causal workload (B=2, H=16, N=8192, d=128) in one call; one head
+    (b=1, h=9) checked in full against the oracle, every other gradient finite."""
+    from blocked_online_softmax_gb300.workloads import CAUSAL_8K as w
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v = make_qkv(B, H, N, d, w.seed)
+    g = dout_like(q, 97)
+    dq, dk, dv = grads_gpu(q, k, v, g, w.scale, True)
+    for t in (dq, dk, dv):
+        assert np.isfinite(t).all()
+    b, h = 1, 9
+    sl = (slice(b, b + 1), slice(h, h + 1))
+    ref = oracle.attention_bwd(q[sl], k[sl], v[sl], g[sl], w.scale, True)
+    check([t[sl] for t in (dq, dk, dv)], ref, "B2H16N8192 head (1, 9)")

@@ -42,6 +42,34 @@ def test_matches_finite_differences(causal):
         np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-8, err_msg=f"d{name}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_lse_gradient_matches_finite_differences(causal):
+    """With a gradient gl on the LSE output too, L = sum(O * dO) + sum(LSE * gl)."""
+    rng = np.random.default_rng(15 + causal)
+    B, H, N, d = 1, 1, 4, 3
+    q, k, v, g = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    gl = rng.standard_normal((B, H, N))
+    scale = 0.9
+
+    def loss(q_, k_, v_):
+        o, lse = oracle.attention(q_, k_, v_, scale, causal)
+        return float((o * g).sum() + (lse * gl).sum())
+
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, scale, causal, dlse=gl)
+    eps = 1e-6
+    for name, grad in (("q", dq), ("k", dk), ("v", dv)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(grad.shape):
+            args_p, args_m = dict(q_=q.copy(), k_=k.copy(), v_=v.copy()), dict(q_=q.copy(), k_=k.copy(), v_=v.copy())
+            args_p[name + "_"][idx] += eps
+            args_m[name + "_"][idx] -= eps
+            num[idx] = (loss(**args_p) - loss(**args_m)) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-8, err_msg=f"d{name}")
+    # the LSE term changes dq and dk but never dv
+    _, _, dv0 = oracle.attention_bwd(q, k, v, g, scale, causal)
+    np.testing.assert_allclose(dv, dv0, rtol=0, atol=0)
+
+
 def test_identical_keys_give_zero_dq():
     """Equal keys make every score row constant in q: dq = 0 (and dS sums to 0 per row)."""
     rng = np.random.default_rng(6)
