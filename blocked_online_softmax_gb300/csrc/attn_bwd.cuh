@@ -8,7 +8,7 @@
 // to see it, recomputes P = exp(S - L) from the saved natural-log LSE, and
 // forms
 //     dV_j += P^T dO_i,   dP = dO_i V_j^T,   dS = P * (dP - D_i) * scale,
-//     dK_j += dS^T Q_i,   dQ_i += dS K_j   (scattered with fp32 atomic adds),
+//     dK_j += dS^T Q_i,   dQ_i += dS K_j   (added into an fp32 buffer),
 // accumulating dK_j and dV_j privately and casting the fp32 dQ buffer to bf16
 // at the end. An optional gradient g on the LSE output enters as D_i - g_i
 // (the derivative of LSE_i in S_ij is P_ij).
@@ -24,18 +24,23 @@
 //                64 columns as bf16 pairs; dV_j += P^T dO_i into X[128,128+d).
 //   Y (warp 10): dP^T = V dO_i^T into Y[0,128); dS^T comes back over its first
 //                64 columns; dK_j += dS^T Q_i into Y[128,128+d); then
-//                dQ_i = dS K_j (fp32) into Y[0,128) for d = 128 (after dK has
-//                read dS^T, in issue order) or into Y[192,256) for d = 64.
+//                dQ_i = dS K_j (fp32, query on the lane) into Y[0,128) for
+//                d = 128 (after dK has read dS^T, in issue order) or into
+//                Y[192,256) for d = 64.
 // Working with the transposes keeps the key on the tensor-memory lane, so the
 // dV and dK products take P^T and dS^T straight from tensor memory.
 // Warps 0-3 (thread = key = lane) form P = exp2(S c - L2) as soon as S^T lands
 // (X can then start dV and the next block's S^T), then dS = P (dP scale -
 // D scale) once dP^T lands; dS also goes to shared memory as [query][key]
 // (128-byte swizzle, K-major), the A operand of the dQ product.
-// Warps 4-7 (thread = query = lane) take dQ_i out of tensor memory and add it
-// into the fp32 accumulation buffer with vector atomics, and stage each block's
-// LSE (base 2) and D (times scale) in shared memory two blocks ahead.
-// Warp 8 issues the TMA loads: K_j and V_j once, Q_i and dO_i into two stages.
+// Warps 4-7 (thread = query = lane) take the dQ part out of tensor memory,
+// write it to shared memory (an 8 KB slot per warp, 128-byte swizzle) and add
+// it into the fp32 dQ buffer with TMA bulk tensor reductions, so the adds move
+// as whole lines; per-thread atomics (one row per lane, or one line per warp
+// with the head dim on the lane) were measured slower. They also stage each
+// block's LSE (base 2) and D (times scale) in shared memory two blocks ahead.
+// Warp 8 issues the TMA loads: K_j and V_j once, Q_i into two stages and dO_i
+// into one (its next load has the dS and dK/dQ steps of a block to land).
 
 namespace bos {
 namespace {
@@ -54,18 +59,20 @@ constexpr int kMaxSmem = 232448;    // 227 KB per CTA
 
 enum : int {
     kBarKV = 0,        // K_j and V_j have landed
-    kBarQFull = 1,     // [2] Q_i and dO_i of a stage have landed
-    kBarQEmpty = 3,    // [2] a stage is free: X's dV and Y's dK of its block are complete (2 commits)
-    kBarSFull = 5,     // S^T of the block is complete (X commit)
-    kBarPReady = 6,    // P^T is written (128 arrivals)
-    kBarDpFull = 7,    // dP^T of the block is complete (Y commit)
-    kBarDsReady = 8,   // dS^T (tensor memory) and dS (shared memory) are written (128 arrivals)
-    kBarDqReady = 9,   // the block's dQ part is complete (Y commit)
-    kBarDqRead = 10,   // the dQ part has been read out of tensor memory (128 arrivals)
-    kBarLseFull = 11,  // [2] LSE and D of a block are staged (128 arrivals)
-    kBarDrainX = 13,   // every MMA of X is complete
-    kBarDrainY = 14,   // every MMA of Y is complete
-    kNumBars = 15,
+    kBarQFull = 1,     // [2] Q_i of a stage has landed
+    kBarQEmpty = 3,    // [2] a Q stage is free: X's S and Y's dK of its block are complete (2 commits)
+    kBarDoFull = 5,    // dO_i has landed
+    kBarDoEmpty = 6,   // the dO buffer is free: X's dV and Y's dP of its block are complete (2 commits)
+    kBarSFull = 7,     // S^T of the block is complete (X commit)
+    kBarPReady = 8,    // P^T is written (128 arrivals)
+    kBarDpFull = 9,    // dP^T of the block is complete (Y commit)
+    kBarDsReady = 10,  // dS^T (tensor memory) and dS (shared memory) are written (128 arrivals)
+    kBarDqReady = 11,  // the block's dQ part is complete (Y commit)
+    kBarDqRead = 12,   // the dQ part has been read out of tensor memory (128 arrivals)
+    kBarLseFull = 13,  // [2] LSE and D of a block are staged (128 arrivals)
+    kBarDrainX = 15,   // every MMA of X is complete
+    kBarDrainY = 16,   // every MMA of Y is complete
+    kNumBars = 17,
 };
 
 template <int D>
@@ -73,10 +80,11 @@ struct Cfg {
     static constexpr int kTile = 128 * D * 2;                  // one bf16 128-row tile
     static constexpr int kBoxes = D / 64;
     static constexpr int kOffK = 0, kOffV = kTile;
-    static constexpr int kOffStage = 2 * kTile;                // stage s: Q_i, then dO_i
-    static constexpr int kStageBytes = 2 * kTile;
-    static constexpr int kOffDS = 6 * kTile;                   // dS, [128 queries][128 keys] bf16: 32 KB
-    static constexpr int kOffLse = kOffDS + 32768;             // [2][128] LSE * log2 e, then [2][128] D * scale
+    static constexpr int kOffQ = 2 * kTile;                    // Q stage s at kOffQ + s * kTile
+    static constexpr int kOffDO = 4 * kTile;
+    static constexpr int kOffDS = 5 * kTile;                   // dS, [128 queries][128 keys] bf16: 32 KB
+    static constexpr int kOffDQ = kOffDS + 32768;              // dQ staging: 8 KB per dQ warp
+    static constexpr int kOffLse = kOffDQ + 32768;             // [2][128] LSE * log2 e, then [2][128] D * scale
     static constexpr int kOffBar = kOffLse + 2048;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // two tensor-memory slots, abort flag
     static constexpr int kUsed = kOffMisc + 16;
@@ -99,6 +107,16 @@ struct BwdArgs {
     uint64_t wait_limit_ns;
 };
 
+// Element-wise add of a shared-memory box into a global tensor (fp32 here),
+// performed by the TMA unit; rows outside the tensor are clipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
@@ -112,25 +130,30 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         tma_load_3d(smem + C::kOffK + b * 16384, tm_k, &bars[kBarKV], b * 64, j * 128, bh);
         tma_load_3d(smem + C::kOffV + b * 16384, tm_v, &bars[kBarKV], b * 64, j * 128, bh);
     }
-    int last[2] = {-1, -1};
+    int last_q[2] = {-1, -1}, last_do = -1;
     for (int it = 0; it < nq; ++it) {
         const int s = it & 1;
-        // the stage's previous block (it - 2) must be released by both issuers
+        // the Q stage's previous block (it - 2) must be released by both issuers
         if (it >= 2 && !wait_or_abort(&bars[kBarQEmpty + s], (uint32_t)(((it >> 1) + 1) & 1), a.wait_limit_ns,
                                       abort_flag))
             break;
-        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&bars[kBarQFull + s], 2 * C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(st + b * 16384, tm_q, &bars[kBarQFull + s], b * 64, (i0 + it) * 128, bh);
-            tma_load_3d(st + C::kTile + b * 16384, tm_do, &bars[kBarQFull + s], b * 64, (i0 + it) * 128, bh);
-        }
-        last[s] = it;
+        mbar_arrive_expect_tx(&bars[kBarQFull + s], C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffQ + s * C::kTile + b * 16384, tm_q, &bars[kBarQFull + s], b * 64,
+                        (i0 + it) * 128, bh);
+        last_q[s] = it;
+        if (it >= 1 && !wait_or_abort(&bars[kBarDoEmpty], (uint32_t)((it - 1) & 1), a.wait_limit_ns, abort_flag))
+            break;
+        mbar_arrive_expect_tx(&bars[kBarDoFull], C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffDO + b * 16384, tm_do, &bars[kBarDoFull], b * 64, (i0 + it) * 128, bh);
+        last_do = it;
     }
     // every copy this thread started must land before the CTA may exit
     mbar_wait(&bars[kBarKV], 0, kDrainLimitNs);
     for (int s = 0; s < 2; ++s)
-        if (last[s] >= 0) mbar_wait(&bars[kBarQFull + s], (uint32_t)((last[s] >> 1) & 1), kDrainLimitNs);
+        if (last_q[s] >= 0) mbar_wait(&bars[kBarQFull + s], (uint32_t)((last_q[s] >> 1) & 1), kDrainLimitNs);
+    if (last_do >= 0) mbar_wait(&bars[kBarDoFull], (uint32_t)(last_do & 1), kDrainLimitNs);
 }
 
 // X: S^T = K Q_i^T, then dV_j += P^T dO_i once P^T is written.
@@ -145,10 +168,10 @@ __device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* 
     // M = 128 keys, N = d, K = 128 queries; A from tensor memory, B (dO) N-major
     constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
     bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
+    const uint32_t sDO = smem_u32(smem + C::kOffDO);
     for (int it = 0; ok && it < nq; ++it) {
         const int s = it & 1;
-        const uint32_t sQ = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        const uint32_t sDO = sQ + C::kTile;
+        const uint32_t sQ = smem_u32(smem + C::kOffQ + s * C::kTile);
         if (!wait_or_abort(&bars[kBarQFull + s], (uint32_t)((it >> 1) & 1), lim, abort_flag)) break;
         tc_fence_after();
         // overwrites P^T of the previous block, which that block's dV (issued earlier) reads
@@ -158,13 +181,16 @@ __device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* 
             mma_ss(tX, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars[kBarSFull]);
-        if (!wait_or_abort(&bars[kBarPReady], (uint32_t)(it & 1), lim, abort_flag)) break;
+        mma_commit(&bars[kBarQEmpty + s]);
+        if (!wait_or_abort(&bars[kBarPReady], (uint32_t)(it & 1), lim, abort_flag) ||
+            !wait_or_abort(&bars[kBarDoFull], (uint32_t)(it & 1), lim, abort_flag))
+            break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // 16 queries per step: 8 columns of bf16 pairs, 16 rows of dO
             mma_ts(tX + kAcc, tX + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), id_kv,
                    (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarQEmpty + s]);
+        mma_commit(&bars[kBarDoEmpty]);
     }
     mma_commit(&bars[kBarDrainX]);
     mbar_wait(&bars[kBarDrainX], 0, kDrainLimitNs);
@@ -184,11 +210,13 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
     // M = 128 queries, N = d, K = 128 keys; A (dS) K-major, B (K_j) N-major
     constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);
     bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
+    const uint32_t sDO = smem_u32(smem + C::kOffDO);
     for (int it = 0; ok && it < nq; ++it) {
         const int s = it & 1;
-        const uint32_t sQ = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        const uint32_t sDO = sQ + C::kTile;
-        if (!wait_or_abort(&bars[kBarQFull + s], (uint32_t)((it >> 1) & 1), lim, abort_flag)) break;
+        const uint32_t sQ = smem_u32(smem + C::kOffQ + s * C::kTile);
+        if (!wait_or_abort(&bars[kBarQFull + s], (uint32_t)((it >> 1) & 1), lim, abort_flag) ||
+            !wait_or_abort(&bars[kBarDoFull], (uint32_t)(it & 1), lim, abort_flag))
+            break;
         if (kDqOverDp && it > 0 && !wait_or_abort(&bars[kBarDqRead], (uint32_t)((it - 1) & 1), lim, abort_flag))
             break;
         tc_fence_after();
@@ -198,6 +226,7 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
             mma_ss(tY, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars[kBarDpFull]);
+        mma_commit(&bars[kBarDoEmpty]);
         if (!wait_or_abort(&bars[kBarDsReady], (uint32_t)(it & 1), lim, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
@@ -344,16 +373,21 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
 }
 
 // Warps 4-7: stage LSE / D two blocks ahead, read each dQ part out of tensor
-// memory (freeing its columns for Y) and add it into the fp32 buffer.
+// memory (freeing its columns for Y) and add it into the fp32 buffer through
+// shared memory and TMA reductions.
 template <int D>
-__device__ void dq_role(uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* bars, volatile int* abort_flag,
-                        int bh, int i0, int nq, const BwdArgs& a) {
+__device__ void dq_role(const CUtensorMap* tm_dq, uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* bars,
+                        volatile int* abort_flag, int bh, int i0, int nq, const BwdArgs& a) {
     using C = Cfg<D>;
     const uint64_t lim = a.wait_limit_ns;
-    const int r = (w & 3) * 32 + lane;                        // tensor-memory lane = query within the block
-    const uint32_t ly = tY + ((uint32_t)((w & 3) * 32) << 16) + C::kTdQ;
+    const int wq = w & 3;
+    const int r = wq * 32 + lane;                             // tensor-memory lane = query within the block
+    const uint32_t ly = tY + ((uint32_t)(wq * 32) << 16) + C::kTdQ;
     float* lse_s = reinterpret_cast<float*>(smem + C::kOffLse);
     float* dsc_s = lse_s + 2 * 128;
+    // this warp's slot: two boxes of [32 rows][32 fp32], each row one 128-byte
+    // line with its 16-byte chunks swizzled by the row (the tensor map's layout)
+    uint8_t* slot = smem + C::kOffDQ + wq * 8192;
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
         bool got = wait_or_abort(bar, parity, lim, abort_flag);
         return __all_sync(0xffffffffu, got);
@@ -369,7 +403,7 @@ __device__ void dq_role(uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* b
     stage(0);
     if (nq > 1) stage(1);
     for (int it = 0; it < nq; ++it) {
-        if (!wait_warp(&bars[kBarDqReady], (uint32_t)(it & 1))) return;
+        if (!wait_warp(&bars[kBarDqReady], (uint32_t)(it & 1))) break;
         tc_fence_after();
         uint32_t v[D];
 #pragma unroll
@@ -380,17 +414,32 @@ __device__ void dq_role(uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* b
         mbar_arrive(&bars[kBarDqRead]);
         // the compute warps finished with this buffer before Y could form this dQ part
         if (it + 2 < nq) stage(it + 2);
-        const int q = (i0 + it) * 128 + r;
-        if (q < a.N) {
-            float* dst = a.dq_acc + ((int64_t)bh * a.N + q) * a.d;
+        const int row0 = (i0 + it) * 128 + wq * 32;           // first query row of this warp
 #pragma unroll
-            for (int e = 0; e < D; e += 4)
-                if (e < a.d)
-                    atomicAdd(reinterpret_cast<float4*>(dst + e),
-                              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
+        for (int h = 0; h < D / 64; ++h) {                    // 64 columns (two boxes) at a time
+            if (lane == 0) bulk_wait_read0();                 // the slot's previous reductions have read it
+            __syncwarp();
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int e = h * 64 + b * 32 + c * 4;
+                    *reinterpret_cast<uint4*>(slot + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                        make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < a.N) {
+                for (int b = 0; b < 2; ++b)
+                    if (h * 64 + b * 32 < a.d) tma_reduce_add_3d(tm_dq, slot + b * 4096, h * 64 + b * 32, row0, bh);
+                bulk_commit();
+            }
         }
     }
+    // the reductions must have read the slot before the CTA exits, and be
+    // complete before the kernel's end hands the buffer to the cast
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
 }
 
 }  // namespace bwd
@@ -400,7 +449,7 @@ template <int D>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
 attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                      const bwd::BwdArgs a) {
+                      const __grid_constant__ CUtensorMap tm_dq, const bwd::BwdArgs a) {
     using C = bwd::Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw;
@@ -426,6 +475,8 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             mbar_init(&bars[bwd::kBarQEmpty + s], 2);
             mbar_init(&bars[bwd::kBarLseFull + s], 128);
         }
+        mbar_init(&bars[bwd::kBarDoFull], 1);
+        mbar_init(&bars[bwd::kBarDoEmpty], 2);
         mbar_init(&bars[bwd::kBarSFull], 1);
         mbar_init(&bars[bwd::kBarPReady], 128);
         mbar_init(&bars[bwd::kBarDpFull], 1);
@@ -442,6 +493,7 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_dq);
     }
     if (warp == bwd::kWarpMmaX) {
         tmem_alloc(tmem_slot, bwd::kCols);
@@ -456,7 +508,7 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (warp < bwd::kWarpDq) {
         bwd::compute_role<D>(tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
     } else if (warp < bwd::kWarpProducer) {
-        bwd::dq_role<D>(tY, warp, lane, smem, bars, abort_flag, bh, i0, nq, a);
+        bwd::dq_role<D>(&tm_dq, tY, warp, lane, smem, bars, abort_flag, bh, i0, nq, a);
     } else if (warp == bwd::kWarpProducer) {
         if (lane == 0) bwd::producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, smem, bars, abort_flag, bh, j, i0, nq, a);
         __syncwarp();
@@ -534,6 +586,23 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, p.d, 128) ||
         !encode_qkv_map(enc, &mv, p.v, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mdo, p.dout, BH, p.N, p.d, 128))
         return ATTN_ERR_BAD_SHAPE;
+    const int64_t rows = (int64_t)BH * p.N;
+    float* dq_acc = static_cast<float*>(p.workspace);
+    const size_t acc_bytes = ((size_t)rows * p.d * sizeof(float) + 255) & ~(size_t)255;
+    float* dsum = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + acc_bytes);
+    // the fp32 dQ buffer [BH, N, d] for the TMA reductions: boxes of 32 rows x
+    // 32 columns (128 bytes, the 128-byte swizzle span)
+    CUtensorMap mdq;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)BH};
+        cuuint64_t strides[2] = {(cuuint64_t)p.d * 4, (cuuint64_t)p.N * p.d * 4};
+        cuuint32_t box[3] = {32, 32, 1};
+        cuuint32_t elem[3] = {1, 1, 1};
+        if (enc(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, elem,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return ATTN_ERR_BAD_SHAPE;
+    }
     static int attr_done[64] = {0};
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         if (cudaFuncSetAttribute(attn_bwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -543,10 +612,6 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
         }
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    const int64_t rows = (int64_t)BH * p.N;
-    float* dq_acc = static_cast<float*>(p.workspace);
-    const size_t acc_bytes = ((size_t)rows * p.d * sizeof(float) + 255) & ~(size_t)255;
-    float* dsum = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + acc_bytes);
     const int64_t pre_blocks = (rows + 7) / 8;   // 8 rows (warps) per 256-thread block
     attn_bwd_pre_kernel<<<(unsigned)(pre_blocks < 1048576 ? pre_blocks : 1048576), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.dlse, dsum, dq_acc, rows,
@@ -567,7 +632,7 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     a.dv = static_cast<__nv_bfloat16*>(p.dv);
     a.wait_limit_ns = g_wait_limit_ns;
     const int64_t grid = (int64_t)BH * a.nkv;
-    attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+    attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     const int64_t n8 = rows * p.d / 8;
     const int64_t post_blocks = (n8 + 255) / 256;

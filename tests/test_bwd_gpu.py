@@ -79,6 +79,18 @@ def test_backward_small(N, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [8, 40, 104])
+def test_backward_other_head_dims(d, causal):
+    """Head dims below each kernel width: partial dQ boxes and zero-filled columns."""
+    q, k, v = make_qkv(1, 2, 300, d, seed=700 + d)
+    g = dout_like(q, 800 + d)
+    scale = float(np.float32(d ** -0.5))
+    gpu = grads_gpu(q, k, v, g, scale, causal)
+    ref = oracle.attention_bwd(q, k, v, g, scale, causal)
+    check(gpu, ref, f"d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_backward_several_blocks(causal):
     q, k, v = make_qkv(2, 3, 700, 128, seed=71)
     g = dout_like(q, 72)
