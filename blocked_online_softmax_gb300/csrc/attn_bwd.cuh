@@ -38,7 +38,9 @@
 // it into the fp32 dQ buffer with TMA bulk tensor reductions, so the adds move
 // as whole lines; per-thread atomics (one row per lane, or one line per warp
 // with the head dim on the lane) were measured slower. They also stage each
-// block's LSE (base 2) and D (times scale) in shared memory two blocks ahead.
+// block's -LSE (base 2) and -D (times scale) in shared memory two blocks ahead,
+// their global loads issued a block before the store; negated, each pair of
+// queries costs the compute warps one packed f32x2 FMA per step.
 // Warp 8 issues the TMA loads: K_j and V_j once, Q_i into two stages and dO_i
 // into one (its next load has the dS and dK/dQ steps of a block to land).
 
@@ -84,7 +86,7 @@ struct Cfg {
     static constexpr int kOffDO = 4 * kTile;
     static constexpr int kOffDS = 5 * kTile;                   // dS, [128 queries][128 keys] bf16: 32 KB
     static constexpr int kOffDQ = kOffDS + 32768;              // dQ staging: 8 KB per dQ warp
-    static constexpr int kOffLse = kOffDQ + 32768;             // [2][128] LSE * log2 e, then [2][128] D * scale
+    static constexpr int kOffLse = kOffDQ + 32768;             // [2][128] -LSE log2 e, then [2][128] -D scale
     static constexpr int kOffBar = kOffLse + 2048;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // two tensor-memory slots, abort flag
     static constexpr int kUsed = kOffMisc + 16;
@@ -115,6 +117,12 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
             reinterpret_cast<uint64_t>(map)),
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -250,7 +258,7 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
 // P^T of one block into tensor memory (over the S^T columns already read) and
 // into registers as bf16 pairs (queries 2e, 2e+1 of each 32-query chunk).
 template <bool kMasked>
-__device__ __forceinline__ void p_phase(uint32_t lx, const float* L, float c2, int r, bool key_ok, bool diag,
+__device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c2x2, int r, bool key_ok, bool diag,
                                         uint32_t (&pk)[64]) {
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
@@ -260,9 +268,10 @@ __device__ __forceinline__ void p_phase(uint32_t lx, const float* L, float c2, i
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int qc = ch * 32 + 2 * e;
-            const float2 l2 = *reinterpret_cast<const float2*>(L + qc);
-            float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, -l2.x));
-            float p1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -l2.y));
+            const uint64_t nl = *reinterpret_cast<const uint64_t*>(nL + qc);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl), x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
             if (kMasked) {
                 if (!key_ok || (diag && qc < r)) p0 = 0.f;
                 if (!key_ok || (diag && qc + 1 < r)) p1 = 0.f;
@@ -281,12 +290,16 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
     const uint64_t lim = a.wait_limit_ns;
     const int r = w * 32 + lane;                              // tensor-memory lane = key within the block
     const uint32_t lx = tX + ((uint32_t)(w * 32) << 16), ly = tY + ((uint32_t)(w * 32) << 16);
-    const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffLse);   // [2][128]
-    const float* dsc_s = lse_s + 2 * 128;                                      // [2][128]
+    const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffLse);   // [2][128] -LSE log2 e
+    const float* dsc_s = lse_s + 2 * 128;                                      // [2][128] -D scale
     // this thread's key in the [query][key] dS buffer: box r / 64, 16-byte chunk
     // (r % 64) / 8 (swizzled with the query row), element r % 8
     uint8_t* ds_col = smem + C::kOffDS + (r >> 6) * 16384 + (r & 7) * 2;
     const int ds_chunk = (r & 63) >> 3;
+    uint32_t dsoff[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dsoff[k] = (uint32_t)((ds_chunk ^ k) << 4);
+    const uint64_t c2x2 = f2_pack(a.c2, a.c2), scale2 = f2_pack(a.scale, a.scale);
     const int key = j * 128 + r;
     const bool key_ok = key < a.N;
     const bool tail_block = j * 128 + 128 > a.N;
@@ -305,9 +318,9 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
         const bool diag = a.causal && it == 0;               // the first query block is block j itself
         uint32_t pk[64];
         if (diag || tail_block)
-            p_phase<true>(lx, L, a.c2, r, key_ok, diag, pk);
+            p_phase<true>(lx, L, c2x2, r, key_ok, diag, pk);
         else
-            p_phase<false>(lx, L, a.c2, r, key_ok, diag, pk);
+            p_phase<false>(lx, L, c2x2, r, key_ok, diag, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kBarPReady]);
@@ -322,18 +335,20 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int qc = ch * 32 + 2 * e;
-                const float2 dd = *reinterpret_cast<const float2*>(Dsc + qc);
+                const uint64_t nd = *reinterpret_cast<const uint64_t*>(Dsc + qc);
                 const uint32_t p = pk[ch * 16 + e];
-                const float ds0 = bf16_lo(p) * fmaf(__uint_as_float(dpv[2 * e]), a.scale, -dd.x);
-                const float ds1 = bf16_hi(p) * fmaf(__uint_as_float(dpv[2 * e + 1]), a.scale, -dd.y);
+                const uint64_t t2 =
+                    f2_fma(f2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), scale2, nd);
+                float ds0, ds1;
+                f2_unpack(f2_mul(f2_pack(bf16_lo(p), bf16_hi(p)), t2), ds0, ds1);
                 dk[e] = pack_bf16(ds0, ds1);
             }
             tmem_st16(ly + ch * 16, dk);                      // dS^T over dP^T columns already read
+            uint8_t* base = ds_col + ch * 32 * 128;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {                    // dS[query][key r], queries 32ch..32ch+31
-                const int qr = ch * 32 + e;
                 const uint32_t pair = dk[e >> 1];
-                *reinterpret_cast<uint16_t*>(ds_col + qr * 128 + ((ds_chunk ^ (qr & 7)) << 4)) =
+                *reinterpret_cast<uint16_t*>(base + e * 128 + dsoff[e & 7]) =
                     (uint16_t)((e & 1) ? (pair >> 16) : (pair & 0xffffu));
             }
         }
@@ -392,17 +407,21 @@ __device__ void dq_role(const CUtensorMap* tm_dq, uint32_t tY, int w, int lane, 
         bool got = wait_or_abort(bar, parity, lim, abort_flag);
         return __all_sync(0xffffffffu, got);
     };
-    auto stage = [&](int it) {
+    auto fetch = [&](int it) -> float2 {
         const int q = (i0 + it) * 128 + r;
+        if (q >= a.N) return make_float2(-INFINITY, 0.f);
+        return make_float2(-(a.lse[(int64_t)bh * a.N + q] * kLog2e), -(a.dsum[(int64_t)bh * a.N + q] * a.scale));
+    };
+    auto stage = [&](int it, float2 val) {
         const int b = it & 1;
-        const bool in = q < a.N;
-        lse_s[b * 128 + r] = in ? a.lse[(int64_t)bh * a.N + q] * kLog2e : INFINITY;
-        dsc_s[b * 128 + r] = in ? a.dsum[(int64_t)bh * a.N + q] * a.scale : 0.f;
+        lse_s[b * 128 + r] = val.x;
+        dsc_s[b * 128 + r] = val.y;
         mbar_arrive(&bars[kBarLseFull + b]);
     };
-    stage(0);
-    if (nq > 1) stage(1);
+    stage(0, fetch(0));
+    if (nq > 1) stage(1, fetch(1));
     for (int it = 0; it < nq; ++it) {
+        const float2 next_val = (it + 2 < nq) ? fetch(it + 2) : make_float2(0.f, 0.f);
         if (!wait_warp(&bars[kBarDqReady], (uint32_t)(it & 1))) break;
         tc_fence_after();
         uint32_t v[D];
@@ -413,7 +432,7 @@ __device__ void dq_role(const CUtensorMap* tm_dq, uint32_t tY, int w, int lane, 
         tc_fence_before();
         mbar_arrive(&bars[kBarDqRead]);
         // the compute warps finished with this buffer before Y could form this dQ part
-        if (it + 2 < nq) stage(it + 2);
+        if (it + 2 < nq) stage(it + 2, next_val);
         const int row0 = (i0 + it) * 128 + wq * 32;           // first query row of this warp
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {                    // 64 columns (two boxes) at a time
