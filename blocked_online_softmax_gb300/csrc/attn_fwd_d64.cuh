@@ -232,7 +232,9 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
     uint8_t* ewarp = sEpit + wq * 32 * 128;   // this warp's 32 rows (4 KB, 1024-byte aligned)
     const int swz = row_in_tile & 7;
     const float c = a.scale_log2;
-    const uint64_t c2 = f2_pack(c, c);
+    // with c == 0 every score is replaced by 0 (mask_row) and scaled by 1
+    const float cs = (c == 0.f) ? 1.f : c;
+    const uint64_t c2 = f2_pack(cs, cs);
     const int total = a.BH * a.U;
     uint32_t s_phase = 0;
     uint32_t blocks = 0;       // blocks of this tile processed so far; PV of block g completes pa/pb phase g
@@ -265,15 +267,11 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             mbar_arrive(s_free);       // the stream may now write S(i+1) over S_t
             const int key0 = j * kBN;
             const bool need_mask = (key0 + kBN > a.N) || (a.causal && key0 + kBN - 1 > tile_row0);
-            int lim = kBN;             // valid keys of this row in this block
-            float m_tile;
-            if (need_mask) {
+            if (need_mask || c == 0.f) {
                 const int last = a.causal ? min(a.N, row + 1) : a.N;
-                lim = max(0, min(kBN, last - key0));
-                m_tile = masked_row_max(sr, c, lim);
-            } else {
-                m_tile = (c >= 0.f) ? row_extreme<true>(sr) * c : row_extreme<false>(sr) * c;
+                mask_row(sr, c, need_mask ? max(0, min(kBN, last - key0)) : kBN);
             }
+            const float m_tile = (cs >= 0.f) ? row_extreme<true>(sr) * cs : row_extreme<false>(sr) * cs;
             // PV of the previous block (phase blocks-1) must be complete before a
             // half of P_t is rewritten (pa: keys 0-63, pb: keys 64-127 and O_t).
             const bool prev = blocks > 0;
@@ -290,8 +288,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             if (prev && !wait_warp(pa_done, par)) { ok = false; break; }
             tc_fence_after();
-            if (need_mask) p_half_to_tmem<true>(sr, 0, c2, negm2, acc, lim, tP);
-            else p_half_to_tmem<false>(sr, 0, c2, negm2, acc, lim, tP);
+            p_half_to_tmem<false>(sr, 0, c2, negm2, acc, kBN, tP);
             // Rescale O_t after the first half of the exponentials, so the wait for
             // the previous block's PV overlaps them; it must land before PV(i).
             bool pb_seen = false;
@@ -313,8 +310,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             mbar_arrive(p_half);
             if (prev && !pb_seen && !wait_warp(pb_done, par)) { ok = false; break; }
             tc_fence_after();
-            if (need_mask) p_half_to_tmem<true>(sr, 1, c2, negm2, acc, lim, tP);
-            else p_half_to_tmem<false>(sr, 1, c2, negm2, acc, lim, tP);
+            p_half_to_tmem<false>(sr, 1, c2, negm2, acc, kBN, tP);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full);

@@ -466,21 +466,18 @@ __device__ __forceinline__ float row_extreme(const uint32_t (&sr)[128]) {
     return reduce8<kMax>(m);
 }
 
-// Max over the first `lim` columns of the scaled scores s * c (keys past a
-// row's last valid key are masked out), 8 chains deep.
-__device__ __forceinline__ float masked_row_max(const uint32_t (&sr)[128], float c, int lim) {
-    float m[8];
+// Masks a score row in place so the unmasked max and exponent code serves
+// masked blocks too (one copy of that code stays hot in the instruction
+// cache; separate masked copies ran once per unit and were fetched cold each
+// time). Columns >= lim become the raw value whose scaled score is -inf
+// (-inf for c > 0, +inf for c < 0). With c == 0 every valid score scales to
+// 0 whatever it is, so valid columns become 0, masked ones -inf, and the
+// caller scales the row by 1 instead (it calls this for every block then).
+__device__ __forceinline__ void mask_row(uint32_t (&sr)[128], float c, int lim) {
+    const uint32_t masked = (c < 0.f) ? 0x7f800000u : 0xff800000u;
+    const uint32_t keep = (c == 0.f) ? 0u : 0xffffffffu;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) m[q] = -INFINITY;
-#pragma unroll
-    for (int cc = 0; cc < 128; cc += 8) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float x = __uint_as_float(sr[cc + q]) * c;
-            m[q] = fmaxf(m[q], (cc + q < lim) ? x : -INFINITY);
-        }
-    }
-    return fmaxf(max3(m[0], m[1], m[2]), max3(m[3], m[4], fmaxf(m[5], fmaxf(m[6], m[7]))));
+    for (int e = 0; e < 128; ++e) sr[e] = (e < lim) ? (sr[e] & keep) : masked;
 }
 
 // exp2 of 32 scores (keys 32*ch .. 32*ch+31): x = s * c - m in one packed FMA per
@@ -560,7 +557,9 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
     uint8_t* pwarp = sPbt + wq * 32 * 128;   // this warp's 32 rows (4 KB, 1024-byte aligned)
     const int swz = row_in_tile & 7;
     const float c = a.scale_log2;
-    const uint64_t c2 = f2_pack(c, c);
+    // with c == 0 every score is replaced by 0 (mask_row) and scaled by 1
+    const float cs = (c == 0.f) ? 1.f : c;
+    const uint64_t c2 = f2_pack(cs, cs);
     const int total = a.BH * a.U;
     uint32_t s_phase = 0, pb_phase = 0;
     bool store_pending = false;   // an O store of this warp may still be reading the P buffer
@@ -592,17 +591,12 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             const int key0 = j * kBN;
             const bool need_mask = (key0 + kBN > a.N) || (a.causal && key0 + kBN - 1 > tile_row0);
             // valid keys of this row in this block: key < N and, causal, key <= row
-            int lim = kBN;
-            float m_tile;
-            if (need_mask) {
+            tmem_ld128(tS, sr);
+            if (need_mask || c == 0.f) {
                 const int last = a.causal ? min(a.N, row + 1) : a.N;
-                lim = max(0, min(kBN, last - key0));
-                tmem_ld128(tS, sr);
-                m_tile = masked_row_max(sr, c, lim);
-            } else {
-                tmem_ld128(tS, sr);
-                m_tile = (c >= 0.f) ? row_extreme<true>(sr) * c : row_extreme<false>(sr) * c;
+                mask_row(sr, c, need_mask ? max(0, min(kBN, last - key0)) : kBN);
             }
+            const float m_tile = (cs >= 0.f) ? row_extreme<true>(sr) * cs : row_extreme<false>(sr) * cs;
             // PV_hi of the previous block must be complete before O_t is rescaled
             // or the shared half of P_t is rewritten.
             bool pb_pending = (i > first);
@@ -620,8 +614,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             // keys 0-63 into tensor memory; the MMA takes them (and then computes the
             // next block's scores) while keys 64-127 are being exponentiated
-            if (need_mask) p_lo_to_tmem<true>(sr, c2, negm2, acc, lim, tS);
-            else p_lo_to_tmem<false>(sr, c2, negm2, acc, lim, tS);
+            p_lo_to_tmem<false>(sr, c2, negm2, acc, kBN, tS);
             // Rescale O_t after the first half of the exponentials, so the wait for
             // the previous block's PV_hi overlaps them; it must land before PV_lo(i).
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -652,8 +645,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 __syncwarp();
                 store_pending = false;
             }
-            if (need_mask) p_hi_to_smem<true>(sr, c2, negm2, acc, lim, prow, swz);
-            else p_hi_to_smem<false>(sr, c2, negm2, acc, lim, prow, swz);
+            p_hi_to_smem<false>(sr, c2, negm2, acc, kBN, prow, swz);
             fence_proxy_async_smem();
             mbar_arrive(p_full);
             const uint64_t s01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
