@@ -37,7 +37,7 @@ ATTN_ERR_TOO_LARGE = 11
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
                     "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version",
-                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes")
+                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided")
 
 _lib = None
 
@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH):
     lib.softmax_rows_fwd.argtypes = [vp, vp, i, i, ctypes.c_longlong, ctypes.c_longlong, vp]
     lib.attn_bwd.restype = i
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, vp]
+    lib.attn_fwd_strided.restype = i
+    lib.attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp, vp, vp, vp, f, i, vp]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     _lib = lib
@@ -123,6 +125,21 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, caus
                                  int(N), int(d), float(scale), int(causal), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
+
+
+def attn_fwd_strided(q, k, v, o, lse, B: int, H: int, N: int, d: int, q_strides, k_strides, v_strides,
+                     o_strides, scale: float, causal, stream=None) -> None:
+    """Enqueue the forward kernel on strided q, k, v, o (C ``attn_fwd_strided``).
+
+    Each ``*_strides`` is three element strides (batch, head, row); the head dim
+    is contiguous. Raises AttnError on a nonzero status.
+    """
+    arrs = [(ctypes.c_longlong * 3)(*[int(x) for x in st]) for st in (q_strides, k_strides, v_strides, o_strides)]
+    st = load_library().attn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                                         int(d), *[ctypes.addressof(a) for a in arrs], float(scale), int(causal),
+                                         _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_strided")
 
 
 def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B: int, H: int, N: int, d: int, scale: float,
@@ -186,6 +203,9 @@ def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal
     """dq, dk, dv (bf16) for the attention() forward outputs o, lse and the gradients dout (and dlse, optional)."""
     import torch
     B, H, N, d = q.shape
+    for t in (q, k, v, o, dout):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 tensors of one [B,H,N,d] shape")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     nbytes = attn_bwd_workspace_bytes(B, H, N, d)
@@ -218,18 +238,33 @@ def softmax(x, out=None, stream=None):
     return out
 
 
-def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None):
-    """O, LSE for bf16 CUDA tensors [B,H,N,d]; scale defaults to 1/sqrt(d) rounded to fp32."""
+def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None, out=None):
+    """O, LSE for bf16 CUDA tensors [B,H,N,d]; scale defaults to 1/sqrt(d) rounded to fp32.
+
+    q, k, v (and ``out``, an optional preallocated O) may be strided views, e.g.
+    [B,N,H,d] tensors transposed to [B,H,N,d], as long as the head dim is
+    contiguous and the other strides are multiples of 8 elements; O is
+    allocated contiguous unless ``out`` is given.
+    """
     import torch
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
         raise ValueError("q, k, v must be [B,H,N,d] with one shape")
     for t in (q, k, v):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise ValueError("q, k, v must be bf16 CUDA tensors")
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    o = torch.empty_like(q)
+    o = torch.empty_like(q, memory_format=torch.contiguous_format) if out is None else out
+    if o.shape != q.shape or o.dtype != torch.bfloat16:
+        raise ValueError("out must be a bf16 tensor shaped like q")
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+    if all(t.is_contiguous() for t in (q, k, v, o)):
+        attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+    else:
+        for t in (q, k, v, o):
+            if t.stride(3) != 1:
+                raise ValueError("the head dim (last) of q, k, v and out must be contiguous")
+        attn_fwd_strided(q, k, v, o, lse, B, H, N, d, *[t.stride()[:3] for t in (q, k, v, o)], scale, causal,
+                         stream)
     return o, lse

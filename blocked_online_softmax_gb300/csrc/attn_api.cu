@@ -82,6 +82,64 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     p.B = B; p.H = H; p.N = N; p.d = d;
     p.scale = scale; p.causal = causal;
+    bos::set_contiguous(p);
+    return bos::launch_attn_fwd(p, static_cast<cudaStream_t>(stream), dev);
+}
+
+namespace {
+
+// Strides (elements) of one [B, H, N, d] operand with a contiguous head dim:
+// positive, and 16-byte multiples (the TMA rule for every global stride).
+bool strides_ok(const long long* s) {
+    for (int i = 0; i < 3; ++i)
+        if (s[i] <= 0 || s[i] % 8 != 0 || s[i] > ((long long)1 << 36)) return false;
+    return true;
+}
+
+// The output must not map two elements to one address: sorted by stride,
+// every dim must start past the extent of the ones inside it.
+bool non_overlapping(const long long* s, int B, int H, int N, int d) {
+    long long st[3] = {s[0], s[1], s[2]}, ext[3] = {B, H, N};
+    for (int i = 0; i < 3; ++i)            // ascending stride (3 elements: insertion sort)
+        for (int j = i; j > 0 && st[j] < st[j - 1]; --j) {
+            long long t = st[j]; st[j] = st[j - 1]; st[j - 1] = t;
+            t = ext[j]; ext[j] = ext[j - 1]; ext[j - 1] = t;
+        }
+    long long span = d;                    // elements covered by the dims inside
+    for (int i = 0; i < 3; ++i) {
+        if (ext[i] == 1) continue;
+        if (st[i] < span) return false;
+        span = st[i] * (ext[i] - 1) + span;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int N, int d, const long long* q_strides, const long long* k_strides,
+                                const long long* v_strides, const long long* o_strides, float scale, int causal,
+                                void* stream) {
+    int st = validate_host(q, k, v, o, lse, B, H, N, d, scale, causal, true);
+    if (st != ATTN_OK) return st;
+    if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_NULLPTR;
+    if (!strides_ok(q_strides) || !strides_ok(k_strides) || !strides_ok(v_strides) || !strides_ok(o_strides))
+        return ATTN_ERR_BAD_ARG;
+    if (q_strides[2] < d || k_strides[2] < d || v_strides[2] < d || !non_overlapping(o_strides, B, H, N, d))
+        return ATTN_ERR_BAD_ARG;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+    bos::AttnParams p;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.B = B; p.H = H; p.N = N; p.d = d;
+    p.scale = scale; p.causal = causal;
+    for (int i = 0; i < 3; ++i) {
+        p.sq[i] = q_strides[i];
+        p.sk[i] = k_strides[i];
+        p.sv[i] = v_strides[i];
+        p.so[i] = o_strides[i];
+    }
     return bos::launch_attn_fwd(p, static_cast<cudaStream_t>(stream), dev);
 }
 
@@ -97,6 +155,7 @@ extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, 
     p.q = q_h; p.k = k_h; p.v = v_h; p.o = o_h; p.lse = lse_h;
     p.B = B; p.H = H; p.N = N; p.d = d;
     p.scale = scale; p.causal = causal;
+    bos::set_contiguous(p);
     return bos::host_forward(p, static_cast<cudaStream_t>(stream_), dev);
 }
 
@@ -172,7 +231,7 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_LAUNCH: return "kernel launch failed";
         case ATTN_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
         case ATTN_ERR_CUDA: return "a CUDA runtime call failed";
-        case ATTN_ERR_BAD_ARG: return "malformed argument (causal must be 0 or 1)";
+        case ATTN_ERR_BAD_ARG: return "malformed argument (causal must be 0 or 1; strides positive multiples of 8, row stride >= d, output not self-overlapping; workspace large enough)";
         case ATTN_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of attn_fwd_host_noalloc (ATTN_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown status";
     }

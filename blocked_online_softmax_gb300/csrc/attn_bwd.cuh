@@ -99,7 +99,7 @@ struct Cfg {
 };
 
 struct BwdArgs {
-    int BH, N, d, nkv, causal;
+    int BH, H, N, d, nkv, causal;
     float scale, c2;                  // c2 = scale * log2 e
     const float* lse;                 // [BH, N] natural log, from the forward pass
     const float* dsum;                // [BH, N] D = rowsum(dO * O) - dLSE
@@ -133,10 +133,11 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
                          const CUtensorMap* tm_do, uint8_t* smem, uint64_t* bars, volatile int* abort_flag,
                          int bh, int j, int i0, int nq, const BwdArgs& a) {
     using C = Cfg<D>;
+    const int bb = bh / a.H, hh = bh - bb * a.H;             // batch and head
     mbar_arrive_expect_tx(&bars[kBarKV], 2 * C::kTile);
     for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_3d(smem + C::kOffK + b * 16384, tm_k, &bars[kBarKV], b * 64, j * 128, bh);
-        tma_load_3d(smem + C::kOffV + b * 16384, tm_v, &bars[kBarKV], b * 64, j * 128, bh);
+        tma_load_4d(smem + C::kOffK + b * 16384, tm_k, &bars[kBarKV], b * 64, j * 128, hh, bb);
+        tma_load_4d(smem + C::kOffV + b * 16384, tm_v, &bars[kBarKV], b * 64, j * 128, hh, bb);
     }
     int last_q[2] = {-1, -1}, last_do = -1;
     for (int it = 0; it < nq; ++it) {
@@ -147,14 +148,14 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
             break;
         mbar_arrive_expect_tx(&bars[kBarQFull + s], C::kTile);
         for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem + C::kOffQ + s * C::kTile + b * 16384, tm_q, &bars[kBarQFull + s], b * 64,
-                        (i0 + it) * 128, bh);
+            tma_load_4d(smem + C::kOffQ + s * C::kTile + b * 16384, tm_q, &bars[kBarQFull + s], b * 64,
+                        (i0 + it) * 128, hh, bb);
         last_q[s] = it;
         if (it >= 1 && !wait_or_abort(&bars[kBarDoEmpty], (uint32_t)((it - 1) & 1), a.wait_limit_ns, abort_flag))
             break;
         mbar_arrive_expect_tx(&bars[kBarDoFull], C::kTile);
         for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem + C::kOffDO + b * 16384, tm_do, &bars[kBarDoFull], b * 64, (i0 + it) * 128, bh);
+            tma_load_4d(smem + C::kOffDO + b * 16384, tm_do, &bars[kBarDoFull], b * 64, (i0 + it) * 128, hh, bb);
         last_do = it;
     }
     // every copy this thread started must land before the CTA may exit
@@ -602,8 +603,12 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     if (!enc) return ATTN_ERR_CUDA;
     const int BH = p.B * p.H;
     CUtensorMap mq, mk, mv, mdo;
-    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, p.d, 128) ||
-        !encode_qkv_map(enc, &mv, p.v, BH, p.N, p.d, 128) || !encode_qkv_map(enc, &mdo, p.dout, BH, p.N, p.d, 128))
+    long long st[3];                                  // dense [B, H, N, d]
+    set_strides(st, (long long)p.H * p.N * p.d, (long long)p.N * p.d, p.d);
+    if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, st, 128) ||
+        !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, st, 128) ||
+        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, st, 128) ||
+        !encode_qkv_map(enc, &mdo, p.dout, p.B, p.H, p.N, p.d, st, 128))
         return ATTN_ERR_BAD_SHAPE;
     const int64_t rows = (int64_t)BH * p.N;
     float* dq_acc = static_cast<float*>(p.workspace);
@@ -638,6 +643,7 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     bwd::BwdArgs a;
     a.BH = BH;
+    a.H = p.H;
     a.N = p.N;
     a.d = p.d;
     a.nkv = (p.N + 127) / 128;

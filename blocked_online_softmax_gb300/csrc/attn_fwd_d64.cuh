@@ -62,10 +62,10 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     uint32_t issued_mask = 0, issued_parity = 0;   // ring loads whose completion is not yet observed
     int q_parity[2] = {-1, -1};                    // per Q buffer: parity of its last load, -1 before any
     bool ok = true;
-    auto load_kv = [&](const CUtensorMap* tm, int j, int bh) -> bool {
+    auto load_kv = [&](const CUtensorMap* tm, int j, int h, int b) -> bool {
         if (!wait_or_abort(&kv_empty[stage], phase ^ 1, a.wait_limit_ns, abort_flag)) return false;
         mbar_arrive_expect_tx(&kv_full[stage], Cfg::kTileBytes);
-        tma_load_3d(sKV + stage * Cfg::kTileBytes, tm, &kv_full[stage], 0, j * kBN, bh);
+        tma_load_4d(sKV + stage * Cfg::kTileBytes, tm, &kv_full[stage], 0, j * kBN, h, b);
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == Cfg::kStages) { stage = 0; phase ^= 1; }
@@ -91,13 +91,13 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         mbar_arrive_expect_tx(&bars[kBarQFull + qb], 2 * Cfg::kTileBytes);
         q_parity[qb] = (r >> 1) & 1;
         for (int t = 0; t < 2; ++t)
-            tma_load_3d(sQ + (qb * 2 + t) * Cfg::kTileBytes, tm_q, &bars[kBarQFull + qb], 0, u.row0 + t * kBM,
-                        u.bh);
+            tma_load_4d(sQ + (qb * 2 + t) * Cfg::kTileBytes, tm_q, &bars[kBarQFull + qb], 0, u.row0 + t * kBM,
+                        u.h, u.b);
         // key block i is j = n-1-i; K runs one block ahead of V
-        if (!load_kv(tm_k, u.n - 1, u.bh)) { ok = false; break; }
+        if (!load_kv(tm_k, u.n - 1, u.h, u.b)) { ok = false; break; }
         for (int i = 0; i < u.n && ok; ++i) {
-            if (i + 1 < u.n && !load_kv(tm_k, u.n - 2 - i, u.bh)) { ok = false; break; }
-            if (!load_kv(tm_v, u.n - 1 - i, u.bh)) { ok = false; break; }
+            if (i + 1 < u.n && !load_kv(tm_k, u.n - 2 - i, u.h, u.b)) { ok = false; break; }
+            if (!load_kv(tm_v, u.n - 1 - i, u.h, u.b)) { ok = false; break; }
         }
     }
     for (int s = 0; s < Cfg::kStages; ++s)
@@ -347,7 +347,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {   // this warp's 32 rows; the next epilogue waits for the read
-            tma_store_3d(tm_o, ewarp, 0, tile_row0 + wq * 32, u.bh);
+            tma_store_4d(tm_o, ewarp, 0, tile_row0 + wq * 32, u.h, u.b);
             bulk_commit();
         }
         __syncwarp();

@@ -117,7 +117,7 @@ struct Cfg {
 };
 
 struct KernelArgs {
-    int BH, N, U, causal;
+    int BH, H, N, U, causal;
     float scale_log2;
     __nv_bfloat16* o;
     float* lse;
@@ -163,7 +163,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
 
 // Decoded work unit.
 struct Unit {
-    int bh, row0, n, first0;   // n key tiles for Q tile 1; Q tile 0 starts at iteration first0
+    int bh, b, h, row0, n, first0;   // n key tiles for Q tile 1; Q tile 0 starts at iteration first0
 };
 
 __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
@@ -176,6 +176,8 @@ __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
         u.bh = k / a.U;
         q = k % a.U;
     }
+    u.b = u.bh / a.H;
+    u.h = u.bh - u.b * a.H;
     u.row0 = q * kUnitRows;
     const int nkv = (a.N + kBN - 1) / kBN;
     int c0 = nkv, c1 = nkv;
@@ -235,11 +237,11 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     int q_parity = -1;                    // parity of the last Q load's phase, -1 before any
     bool ok = true;
     // One K/V tile into the next ring stage.
-    auto load_kv = [&](const CUtensorMap* tm, int j, int bh) -> bool {
+    auto load_kv = [&](const CUtensorMap* tm, int j, const Unit& u) -> bool {
         if (!wait_or_abort(&kv_empty[stage], phase ^ 1, a.wait_limit_ns, abort_flag)) return false;
         mbar_arrive_expect_tx(&kv_full[stage], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(sKV + stage * C::kTileBytes + b * 16384, tm, &kv_full[stage], b * 64, j * kBN, bh);
+            tma_load_4d(sKV + stage * C::kTileBytes + b * 16384, tm, &kv_full[stage], b * 64, j * kBN, u.h, u.b);
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -266,11 +268,11 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         q_parity = r & 1;
         for (int t = 0; t < 2; ++t)
             for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_3d(sQ + t * C::kTileBytes + b * 16384, tm_q, &bars[kBarQFull], b * 64, u.row0 + t * kBM,
-                            u.bh);
+                tma_load_4d(sQ + t * C::kTileBytes + b * 16384, tm_q, &bars[kBarQFull], b * 64, u.row0 + t * kBM,
+                            u.h, u.b);
         for (int i = 0; i < u.n && ok; ++i) {
             const int j = u.n - 1 - i;
-            if (!load_kv(tm_k, j, u.bh) || !load_kv(tm_v, j, u.bh)) { ok = false; break; }
+            if (!load_kv(tm_k, j, u) || !load_kv(tm_v, j, u)) { ok = false; break; }
         }
     }
     // Every copy this thread started must land before the CTA may exit (on the
@@ -682,7 +684,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {   // this warp's 32 rows
-                tma_store_3d(tm_o, pwarp, s * 64, tile_row0 + wq * 32, u.bh);
+                tma_store_4d(tm_o, pwarp, s * 64, tile_row0 + wq * 32, u.h, u.b);
                 bulk_commit();
             }
             __syncwarp();
@@ -821,15 +823,17 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); boxes of 64 columns x
-// `rows` rows, 128-byte swizzle; loads read rows past N (and columns past d) as
-// zero, stores drop them.
-bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int BH, int N, int d, int rows) {
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-    cuuint32_t elem[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+// bf16 [B, H, N, d] with element strides st = {batch, head, row} (d
+// contiguous) viewed as a 4-D tensor (column, row, head, batch); boxes of 64
+// columns x `rows` rows, 128-byte swizzle; loads read rows past N (and columns
+// past d) as zero, stores drop them.
+bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int B, int H, int N, int d,
+                    const long long (&st)[3], int rows) {
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
+    cuuint32_t elem[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, elem,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -849,8 +853,10 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     // Q, K and V move in 128-row boxes; O is stored 32 rows (one warp) at a time
     // (the maps describe the caller's d columns; boxes are 64 wide, so columns
     // from d up to the kernel's width D load as zero and are not stored)
-    if (!encode_qkv_map(enc, &mq, p.q, BH, p.N, p.d, kBM) || !encode_qkv_map(enc, &mk, p.k, BH, p.N, p.d, kBN) ||
-        !encode_qkv_map(enc, &mv, p.v, BH, p.N, p.d, kBN) || !encode_qkv_map(enc, &mo, p.o, BH, p.N, p.d, 32))
+    if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, p.sq, kBM) ||
+        !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, p.sk, kBN) ||
+        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, p.sv, kBN) ||
+        !encode_qkv_map(enc, &mo, p.o, p.B, p.H, p.N, p.d, p.so, 32))
         return ATTN_ERR_BAD_SHAPE;
     static int sms_cache[64] = {0};
     static int attr_done[64] = {0};
@@ -882,6 +888,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     }
     KernelArgs a;
     a.BH = BH;
+    a.H = p.H;
     a.N = p.N;
     a.U = (p.N + kUnitRows - 1) / kUnitRows;
     a.causal = p.causal;

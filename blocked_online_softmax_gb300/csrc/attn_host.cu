@@ -114,6 +114,7 @@ int host_forward(const AttnParams& p, cudaStream_t caller, int dev) {
         cp.lse = reinterpret_cast<float*>(base + off_l + ol);
         cp.B = 1;
         cp.H = nh;
+        set_contiguous(cp);
         rc = launch_attn_fwd(cp, hs.s_comp, dev);
         if (rc != ATTN_OK) break;
         ok = cudaEventRecord(hs.ev_comp[c], hs.s_comp) == cudaSuccess &&

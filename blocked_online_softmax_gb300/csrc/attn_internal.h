@@ -17,7 +17,24 @@ struct AttnParams {
     int B, H, N, d;
     float scale;
     int causal;
+    // element strides of the batch, head and row dims of q, k, v, o (the head
+    // dim is contiguous); set_contiguous fills the dense [B, H, N, d] ones
+    long long sq[3], sk[3], sv[3], so[3];
 };
+
+inline void set_strides(long long (&s)[3], long long sb, long long sh, long long sn) {
+    s[0] = sb;
+    s[1] = sh;
+    s[2] = sn;
+}
+
+inline void set_contiguous(AttnParams& p) {
+    const long long sn = p.d, sh = (long long)p.N * p.d, sb = (long long)p.H * p.N * p.d;
+    set_strides(p.sq, sb, sh, sn);
+    set_strides(p.sk, sb, sh, sn);
+    set_strides(p.sv, sb, sh, sn);
+    set_strides(p.so, sb, sh, sn);
+}
 
 // Enqueues the forward kernel for validated arguments on `stream` (device `dev`
 // is current). Returns an attn_status code.

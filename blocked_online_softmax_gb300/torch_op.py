@@ -9,10 +9,11 @@ outputs (and the backward's workspace) and marshals the arguments into
 implementations only state the output shapes. There is no CPU implementation
 (the library has no CPU path).
 
-Autograd: the forward saves q, k, v and its outputs O and LSE; the backward
-passes dL/dO and, when the loss also uses LSE, dL/dLSE to ``attn_bwd`` (the
-derivative of LSE_i in the score S_ij is P_ij, which the kernel folds into its
-row term D). ``scale`` and ``causal`` get no gradient.
+The forward accepts strided q, k, v (head dim contiguous); O comes back
+contiguous. Autograd: the forward saves q, k, v and its outputs O and LSE;
+the backward passes dL/dO and, when the loss also uses LSE, dL/dLSE to
+``attn_bwd`` (the derivative of LSE_i in the score S_ij is P_ij, which the
+kernel folds into its row term D). ``scale`` and ``causal`` get no gradient.
 
     import blocked_online_softmax_gb300.torch_op
     o, lse = torch.ops.bos.attention_fwd(q, k, v, scale, causal)
@@ -39,7 +40,7 @@ def _attention_fwd_fake(q, k, v, scale, causal):
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
         raise ValueError("q, k, v must be [B,H,N,d] with one shape")
     B, H, N, _ = q.shape
-    return torch.empty_like(q), q.new_empty((B, H, N), dtype=torch.float32)
+    return torch.empty(q.shape, dtype=q.dtype, device=q.device), q.new_empty((B, H, N), dtype=torch.float32)
 
 
 @torch.library.custom_op("bos::attention_bwd", mutates_args=(), device_types="cuda")
@@ -65,6 +66,7 @@ def _setup_context(ctx, inputs, output):
 
 def _backward(ctx, grad_o, grad_lse):
     q, k, v, o, lse = ctx.saved_tensors
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()   # the backward takes dense [B,H,N,d]
     if grad_o is None:
         grad_o = torch.zeros_like(o)
     grad_o = grad_o.to(torch.bfloat16).contiguous()

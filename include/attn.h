@@ -76,6 +76,32 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * attn_fwd_strided - attn_fwd on strided (non-contiguous) q, k, v and o, e.g.
+ * the [B, N, H, d] layout a fused projection produces, or rows padded past d.
+ * "Sizing the attention kernel" of "4.4 Writing GPU Kernels with Triton"
+ * passes every tensor's batch, head, row and column strides to the kernel;
+ * here the head dim must be contiguous (stride 1) and the other three are
+ * given per tensor.
+ *
+ *   q_strides, k_strides, v_strides, o_strides : host arrays of 3 element
+ *       strides {batch, head, row}; element (b, h, n, c) of q is at
+ *       q + b*q_strides[0] + h*q_strides[1] + n*q_strides[2] + c. Each stride
+ *       must be a positive multiple of 8 elements (16 bytes, the TMA rule for
+ *       global strides) and at most 2^36; the row stride of q, k and v must be
+ *       >= d; o must not map two elements to one address.
+ *   lse : fp32 [B, H, N], contiguous, as attn_fwd.
+ *   other arguments as attn_fwd (pointers 16-byte aligned, d a multiple of 8
+ *   up to 128).
+ *
+ * Returns the attn_fwd codes; ATTN_ERR_NULLPTR for a NULL stride array,
+ * ATTN_ERR_BAD_ARG for strides that break the rules above. attn_fwd itself is
+ * this call with the dense strides {H*N*d, N*d, d}.
+ */
+int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                     const long long* q_strides, const long long* k_strides, const long long* v_strides,
+                     const long long* o_strides, float scale, int causal, void* stream);
+
+/*
  * attn_fwd_host - the same operation on HOST buffers, end to end.
  *
  *   q_h, k_h, v_h : bf16 host arrays, contiguous [B, H, N, d] (pinned memory

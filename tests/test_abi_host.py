@@ -66,6 +66,36 @@ def test_host_validation_before_any_launch(lib, kw, code):
     assert _call(lib, **kw) == code
 
 
+def _call_strided(lib, qs=(8 * 64, 8 * 64, 64), os_=(8 * 64, 8 * 64, 64), B=1, H=1, N=8, d=64, null=None):
+    arrs = [(ctypes.c_longlong * 3)(*st) for st in (qs, qs, qs, os_)]
+    ptrs = [ctypes.addressof(a) for a in arrs]
+    if null is not None:
+        ptrs[null] = None
+    return lib.attn_fwd_strided(16, 32, 48, 64, 80, B, H, N, d, *ptrs, ctypes.c_float(0.125), 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(null=0), bos.ATTN_ERR_NULLPTR), (dict(null=3), bos.ATTN_ERR_NULLPTR),
+    (dict(qs=(512, 512, 60)), bos.ATTN_ERR_BAD_ARG),          # row stride not a multiple of 8
+    (dict(qs=(512, 0, 64)), bos.ATTN_ERR_BAD_ARG),            # zero stride
+    (dict(qs=(512, 512, 56)), bos.ATTN_ERR_BAD_ARG),          # rows overlap in the head dim
+    (dict(os_=(512, 512, 56)), bos.ATTN_ERR_BAD_ARG),         # output rows overlap
+    (dict(os_=(64, 64, 8), B=2, H=2, N=8, d=8), bos.ATTN_ERR_BAD_ARG),   # output (b, h) planes overlap
+    (dict(qs=(1 << 40, 512, 64)), bos.ATTN_ERR_BAD_ARG),      # past the TMA stride range
+])
+def test_strided_validation(lib, kw, code):
+    assert _call_strided(lib, **kw) == code
+
+
+def test_strided_accepts_transposed_layouts(lib):
+    """[B, N, H, d] viewed as [B, H, N, d]: rows H*d apart, heads d apart. With
+    valid strides the call only fails for want of a GPU, after validation."""
+    B, H, N, d = 2, 4, 8, 64
+    bnhd = (N * H * d, d, H * d)
+    st = _call_strided(lib, qs=bnhd, os_=bnhd, B=B, H=H, N=N, d=d)
+    assert st not in (bos.ATTN_ERR_BAD_ARG, bos.ATTN_ERR_NULLPTR, bos.ATTN_ERR_MISALIGNED)
+
+
 def test_host_entry_validation(lib):
     st = lib.attn_fwd_host(None, 8, 8, 8, 8, 1, 1, 4, 64, ctypes.c_float(1.0), 0, None)
     assert st == bos.ATTN_ERR_NULLPTR

@@ -201,3 +201,51 @@ def test_workload_full_size_sampled(w):
     o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
     d = w.d
     assert_parity(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.name)
+
+
+# ------------------------------------------------------------------ strided layouts
+
+def _layout(x, kind, pad=16):
+    """x: host [B,H,N,d]. Returns a device view of the same values in the layout
+    `kind` ("bnhd": a [B,N,H,d] tensor transposed; "padded": rows padded past d)
+    and the backing tensor."""
+    B, H, N, d = x.shape
+    if kind == "bnhd":
+        base = x.permute(0, 2, 1, 3).contiguous().cuda()
+        return base.permute(0, 2, 1, 3), base
+    base = torch.zeros(B, H, N, d + pad, dtype=x.dtype).cuda()
+    base[..., :d] = x.cuda()
+    return base[..., :d], base
+
+
+@pytest.mark.parametrize("d,causal,N", [(128, True, 333), (128, False, 300), (64, True, 257), (40, False, 200)])
+@pytest.mark.parametrize("kind", ["bnhd", "padded"])
+def test_strided_layouts(kind, d, causal, N):
+    """attn_fwd_strided on [B,N,H,d] views and on rows padded past d, inputs and
+    output: equal to the oracle, and the output's padding is never written."""
+    B, H = 2, 3
+    q, k, v = make_qkv(B, H, N, d, seed=60 + d + N)
+    scale = float(np.float32(d ** -0.5))
+    (qd, _), (kd, _), (vd, _) = (_layout(t, kind) for t in (q, k, v))
+    sentinel = torch.full((B, H, N, d), SENT_BF16, dtype=torch.bfloat16)
+    od, obase = _layout(sentinel, kind)
+    if kind == "padded":
+        obase[..., d:] = SENT_BF16
+    assert not qd.is_contiguous() and not od.is_contiguous()
+    o, lse = bos.attention(qd, kd, vd, scale=scale, causal=causal, out=od)
+    torch.cuda.synchronize()
+    assert o.data_ptr() == od.data_ptr()
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"{kind} d={d} causal={causal}")
+    if kind == "padded":
+        assert torch.all(obase[..., d:].float().cpu() == SENT_BF16), "wrote into the row padding of O"
+
+
+def test_strided_matches_contiguous_bitwise():
+    """The strided entry on a transposed copy gives the contiguous call's bytes."""
+    q, k, v = make_qkv(1, 4, 700, 128, seed=66)
+    o1, l1 = bos.attention(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    (qd, _), (kd, _), (vd, _) = (_layout(t, "bnhd") for t in (q, k, v))
+    o2, l2 = bos.attention(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
