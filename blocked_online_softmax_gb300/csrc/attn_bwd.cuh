@@ -74,7 +74,8 @@ enum : int {
     kBarLseFull = 13,  // [2] LSE and D of a block are staged (128 arrivals)
     kBarDrainX = 15,   // every MMA of X is complete
     kBarDrainY = 16,   // every MMA of Y is complete
-    kNumBars = 17,
+    kBarDsHalf = 17,   // dS^T of queries 0-63 is written (128 arrivals): Y may start dK
+    kNumBars = 18,
 };
 
 template <int D>
@@ -236,12 +237,18 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
         }
         mma_commit(&bars[kBarDpFull]);
         mma_commit(&bars[kBarDoEmpty]);
+        // dK over queries 0-63 as soon as their dS^T is written, the rest once all of dS is
+        if (!wait_or_abort(&bars[kBarDsHalf], (uint32_t)(it & 1), lim, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tY + kAcc, tY + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv,
+                   (it > 0 || kk > 0) ? 1u : 0u);
         if (!wait_or_abort(&bars[kBarDsReady], (uint32_t)(it & 1), lim, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tY + kAcc, tY + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 4; kk < 8; ++kk)
+            mma_ts(tY + kAcc, tY + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv, 1u);
         mma_commit(&bars[kBarQEmpty + s]);
         if (!kDqOverDp && it > 0 && !wait_or_abort(&bars[kBarDqRead], (uint32_t)((it - 1) & 1), lim, abort_flag))
             break;
@@ -351,6 +358,11 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
                 const uint32_t pair = dk[e >> 1];
                 *reinterpret_cast<uint16_t*>(base + e * 128 + dsoff[e & 7]) =
                     (uint16_t)((e & 1) ? (pair >> 16) : (pair & 0xffffu));
+            }
+            if (ch == 1) {                                    // Y's first four dK steps need only these
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars[kBarDsHalf]);
             }
         }
         tmem_st_wait();
@@ -505,6 +517,7 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_init(&bars[bwd::kBarDqRead], 128);
         mbar_init(&bars[bwd::kBarDrainX], 1);
         mbar_init(&bars[bwd::kBarDrainY], 1);
+        mbar_init(&bars[bwd::kBarDsHalf], 128);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -549,19 +562,24 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
 }
 
-// D = rowsum(dO * O) - dLSE in fp32 per row, and the fp32 dQ buffer zeroed. One
-// warp per row; lane l covers columns 8l..8l+7 (d is a multiple of 8 up to 128).
+// D = rowsum(dO * O) - dLSE in fp32 per row, and the fp32 dQ buffer zeroed.
+// A row is d / 8 lanes (16-byte loads of 8 bf16), so one warp covers
+// 32 / (d / 8) rows at a time (two at d = 128, four at d = 64); grid-stride.
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                            const __nv_bfloat16* __restrict__ dout,
                                                            const float* __restrict__ dlse,
                                                            float* __restrict__ dsum, float* __restrict__ dq_acc,
                                                            int64_t rows, int d) {
     const int lane = threadIdx.x % 32;
-    const int c = lane * 8;
-    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; row < rows;
-         row += (int64_t)gridDim.x * blockDim.x / 32) {
+    const int lanes_per_row = d <= 8 ? 1 : d <= 16 ? 2 : d <= 32 ? 4 : d <= 64 ? 8 : 16;
+    const int rows_per_warp = 32 / lanes_per_row;
+    const int sub = lane / lanes_per_row, c = (lane % lanes_per_row) * 8;
+    const int64_t warps = (int64_t)gridDim.x * blockDim.x / 32;
+    for (int64_t row0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32 * rows_per_warp; row0 < rows;
+         row0 += warps * rows_per_warp) {
+        const int64_t row = row0 + sub;
         float s = 0.f;
-        if (c < d) {
+        if (row < rows && c < d) {
             const uint4 ov = *reinterpret_cast<const uint4*>(o + row * d + c);
             const uint4 gv = *reinterpret_cast<const uint4*>(dout + row * d + c);
             const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -572,19 +590,18 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* 
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) dsum[row] = dlse ? s - dlse[row] : s;
+        for (int off = lanes_per_row / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (row < rows && lane % lanes_per_row == 0) dsum[row] = dlse ? s - dlse[row] : s;
     }
 }
 
-// dQ: the fp32 accumulation buffer to bf16, eight values per thread (n % 8 == 0).
+// dQ: the fp32 accumulation buffer to bf16, eight values per step (n % 8 == 0); grid-stride.
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restrict__ dq_acc,
                                                             __nv_bfloat16* __restrict__ dq, int64_t n8) {
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
-        const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(dq_acc) + 2 * idx);
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(dq_acc) + 2 * idx + 1);
         uint4 w;
         w.x = pack_bf16(a.x, a.y);
         w.y = pack_bf16(a.z, a.w);
@@ -636,8 +653,20 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
         }
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    const int64_t pre_blocks = (rows + 7) / 8;   // 8 rows (warps) per 256-thread block
-    attn_bwd_pre_kernel<<<(unsigned)(pre_blocks < 1048576 ? pre_blocks : 1048576), 256, 0, stream>>>(
+    static int sms_cache[64] = {0};
+    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+    }
+    // the two element-wise passes: grid-stride, 8 blocks of 256 threads per SM
+    const int64_t pre_rows_per_block = 8 * (32 / (p.d <= 8 ? 1 : p.d <= 16 ? 2 : p.d <= 32 ? 4 : p.d <= 64 ? 8 : 16));
+    const int64_t pre_need = (rows + pre_rows_per_block - 1) / pre_rows_per_block;
+    const int64_t pre_blocks = pre_need < (int64_t)sms * 8 ? pre_need : (int64_t)sms * 8;
+    attn_bwd_pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.dlse, dsum, dq_acc, rows,
         p.d);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
@@ -660,8 +689,9 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     const int64_t n8 = rows * p.d / 8;
-    const int64_t post_blocks = (n8 + 255) / 256;
-    attn_bwd_post_kernel<<<(unsigned)(post_blocks < 1048576 ? post_blocks : 1048576), 256, 0, stream>>>(
+    const int64_t post_need = (n8 + 255) / 256;
+    const int64_t post_blocks = post_need < (int64_t)sms * 8 ? post_need : (int64_t)sms * 8;
+    attn_bwd_post_kernel<<<(unsigned)post_blocks, 256, 0, stream>>>(
         dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
