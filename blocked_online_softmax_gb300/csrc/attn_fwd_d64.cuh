@@ -202,13 +202,12 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
 }
 
 // Keys 64h .. 64h+63 of P_t (chunks 2h and 2h+1) into P_t's tensor-memory columns.
-template <bool kMasked>
 __device__ __forceinline__ void p_half_to_tmem(const uint32_t (&sr)[128], int h, uint64_t c2, uint64_t negm2,
-                                               uint64_t (&acc)[4], int lim, uint32_t tP) {
+                                               uint64_t (&acc)[4], uint32_t tP) {
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
-        exp_pack<kMasked>(sr, 2 * h + cc, c2, negm2, acc, lim, pk);
+        exp_pack(sr, 2 * h + cc, c2, negm2, acc, pk);
         tmem_st16(tP + (2 * h + cc) * 16, pk);
     }
 }
@@ -288,7 +287,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             if (prev && !wait_warp(pa_done, par)) { ok = false; break; }
             tc_fence_after();
-            p_half_to_tmem<false>(sr, 0, c2, negm2, acc, kBN, tP);
+            p_half_to_tmem(sr, 0, c2, negm2, acc, tP);
             // Rescale O_t after the first half of the exponentials, so the wait for
             // the previous block's PV overlaps them; it must land before PV(i).
             bool pb_seen = false;
@@ -310,7 +309,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             mbar_arrive(p_half);
             if (prev && !pb_seen && !wait_warp(pb_done, par)) { ok = false; break; }
             tc_fence_after();
-            p_half_to_tmem<false>(sr, 1, c2, negm2, acc, kBN, tP);
+            p_half_to_tmem(sr, 1, c2, negm2, acc, tP);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full);

@@ -483,49 +483,42 @@ __device__ __forceinline__ void mask_row(uint32_t (&sr)[128], float c, int lim) 
 }
 
 // exp2 of 32 scores (keys 32*ch .. 32*ch+31): x = s * c - m in one packed FMA per
-// pair, p = 2^x (0 for columns >= lim when kMasked), packed into 16 bf16 pairs
-// (key 2e in the low half of pk[e]); the fp32 probabilities are added pairwise
-// into acc[4].
-template <bool kMasked>
+// pair, p = 2^x (masked columns hold the raw value whose x is -inf, see
+// mask_row), packed into 16 bf16 pairs (key 2e in the low half of pk[e]); the
+// fp32 probabilities are added pairwise into acc[4].
 __device__ __forceinline__ void exp_pack(const uint32_t (&sr)[128], int ch, uint64_t c2, uint64_t negm2,
-                                         uint64_t (&acc)[4], int lim, uint32_t (&pk)[16]) {
+                                         uint64_t (&acc)[4], uint32_t (&pk)[16]) {
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
         const int c0 = ch * 32 + 2 * e;
         const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), c2, negm2);
         float x0, x1;
         f2_unpack(x2, x0, x1);
-        float p0 = ex2(x0), p1 = ex2(x1);
-        if (kMasked) {
-            p0 = (c0 < lim) ? p0 : 0.f;
-            p1 = (c0 + 1 < lim) ? p1 : 0.f;
-        }
+        const float p0 = ex2(x0), p1 = ex2(x1);
         acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
         pk[e] = pack_bf16(p0, p1);
     }
 }
 
 // Keys 0-63 of P_t: chunks 0 and 1 into tensor memory (over S_t's first 32 columns).
-template <bool kMasked>
 __device__ __forceinline__ void p_lo_to_tmem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
-                                             uint64_t (&acc)[4], int lim, uint32_t tS) {
+                                             uint64_t (&acc)[4], uint32_t tS) {
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         uint32_t pk[16];
-        exp_pack<kMasked>(sr, ch, c2, negm2, acc, lim, pk);
+        exp_pack(sr, ch, c2, negm2, acc, pk);
         tmem_st16(tS + ch * 16, pk);
     }
 }
 
 // Keys 64-127 of P_t: chunks 2 and 3 into this row of the shared-memory half,
 // K-major with the 128-byte swizzle (16-byte chunk q of the row at q ^ (row & 7)).
-template <bool kMasked>
 __device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
-                                             uint64_t (&acc)[4], int lim, uint8_t* prow, int swz) {
+                                             uint64_t (&acc)[4], uint8_t* prow, int swz) {
 #pragma unroll
     for (int ch = 2; ch < 4; ++ch) {
         uint32_t pk[16];
-        exp_pack<kMasked>(sr, ch, c2, negm2, acc, lim, pk);
+        exp_pack(sr, ch, c2, negm2, acc, pk);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int c16 = (ch - 2) * 4 + q;
@@ -616,7 +609,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             // keys 0-63 into tensor memory; the MMA takes them (and then computes the
             // next block's scores) while keys 64-127 are being exponentiated
-            p_lo_to_tmem<false>(sr, c2, negm2, acc, kBN, tS);
+            p_lo_to_tmem(sr, c2, negm2, acc, tS);
             // Rescale O_t after the first half of the exponentials, so the wait for
             // the previous block's PV_hi overlaps them; it must land before PV_lo(i).
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -647,7 +640,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 __syncwarp();
                 store_pending = false;
             }
-            p_hi_to_smem<false>(sr, c2, negm2, acc, kBN, prow, swz);
+            p_hi_to_smem(sr, c2, negm2, acc, prow, swz);
             fence_proxy_async_smem();
             mbar_arrive(p_full);
             const uint64_t s01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
