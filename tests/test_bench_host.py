@@ -1,0 +1,39 @@
+"""bench.py's host-side bookkeeping (no GPU): the roofline's traffic figure is
+used only while the kernel sources match the capture it came from, the clock
+record flags throttling, and the metric arithmetic is what the line claims."""
+import bench
+
+
+def test_traffic_only_for_the_captured_source(monkeypatch):
+    text = open(bench.os.path.join(bench.ROOT, "profiles",
+                                   "attn_fwd_causal_b2h16n8192d128_traffic.txt")).read()
+    fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
+    sha = fields["kernel_source_sha"].strip()
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: sha)
+    assert bench.recorded_traffic("causal_b2h16n8192d128") == float(fields["dram_bytes_per_launch"])
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.recorded_traffic("causal_b2h16n8192d128") is None
+    assert bench.recorded_traffic("no_such_workload") is None
+
+
+def test_kernel_source_hash_is_stable():
+    assert bench.kernel_source_hash() == bench.kernel_source_hash()
+    assert len(bench.kernel_source_hash()) == 16
+
+
+def test_clock_summary_flags_throttling():
+    # index, sm MHz, max MHz, power, active reasons, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
+    idle = ["0", "345", "2070", "100.0", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    busy = ["0", "2070", "2070", "450.5", "0x4", "Not Active", "Not Active", "Not Active", "Active"]
+    slow = ["0", "1500", "2070", "300.0", "0x8", "Active", "Not Active", "Not Active", "Not Active"]
+    s = bench.ClockSampler.summarise([idle, busy, busy, busy])
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 4 and s["power_w_max"] == 450.5
+    s = bench.ClockSampler.summarise([busy, slow, slow])
+    assert "hw_slowdown" in s["reasons"] and s["sm_mhz"] == 1500.0
+    assert bench.ClockSampler.summarise([])["reasons"] == ["unsampled"]
+
+
+def test_job_throughput_is_whole_job_flops_per_second():
+    # 2 ranks x 10 steps x 1e12 FLOP in 4 s: 5 TFLOP/s for the job
+    assert abs(bench.job_throughput(1e12, steps=10, world=2, seconds=4.0) - 5.0) < 1e-12
