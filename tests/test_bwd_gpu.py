@@ -145,3 +145,15 @@ def test_backward_full_size_sampled_head():
     sl = (slice(b, b + 1), slice(h, h + 1))
     ref = oracle.attention_bwd(q[sl], k[sl], v[sl], g[sl], w.scale, True)
     check([t[sl] for t in (dq, dk, dv)], ref, "B2H16N8192 head (1, 9)")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("scale", [0.0, -0.2])
+def test_backward_zero_and_negative_scale(scale, causal):
+    """Scale 0 (uniform attention over the valid keys) and a negative scale,
+    with a ragged tail: the masked blocks must still drop the invalid keys."""
+    q, k, v = make_qkv(1, 2, 300, 128, seed=85)
+    g = dout_like(q, 86)
+    gpu = grads_gpu(q, k, v, g, scale, causal)
+    ref = oracle.attention_bwd(q, k, v, g, scale, causal)
+    check(gpu, ref, f"scale={scale} causal={causal}")
