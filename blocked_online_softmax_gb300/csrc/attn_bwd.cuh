@@ -75,7 +75,8 @@ enum : int {
     kBarDrainX = 15,   // every MMA of X is complete
     kBarDrainY = 16,   // every MMA of Y is complete
     kBarDsHalf = 17,   // dS^T of queries 0-63 is written (128 arrivals): Y may start dK
-    kNumBars = 18,
+    kBarNever = 18,    // test hook: nothing arrives on it
+    kNumBars = 19,
 };
 
 template <int D>
@@ -108,6 +109,7 @@ struct BwdArgs {
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     uint64_t wait_limit_ns;
+    int test_stall;                   // test hook: X first waits on a barrier nothing signals
 };
 
 // Element-wise add of a shared-memory box into a global tensor (fp32 here),
@@ -177,7 +179,8 @@ __device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* 
     constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
     // M = 128 keys, N = d, K = 128 queries; A from tensor memory, B (dO) N-major
     constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
-    bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
+    bool ok = !(a.test_stall && !wait_or_abort(&bars[kBarNever], 0, lim, abort_flag)) &&
+              wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
     const uint32_t sDO = smem_u32(smem + C::kOffDO);
     for (int it = 0; ok && it < nq; ++it) {
         const int s = it & 1;
@@ -518,6 +521,7 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_init(&bars[bwd::kBarDrainX], 1);
         mbar_init(&bars[bwd::kBarDrainY], 1);
         mbar_init(&bars[bwd::kBarDsHalf], 128);
+        mbar_init(&bars[bwd::kBarNever], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -685,6 +689,7 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     a.dk = static_cast<__nv_bfloat16*>(p.dk);
     a.dv = static_cast<__nv_bfloat16*>(p.dv);
     a.wait_limit_ns = g_wait_limit_ns;
+    a.test_stall = g_test_stall;
     const int64_t grid = (int64_t)BH * a.nkv;
     attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;

@@ -172,8 +172,8 @@ int attn_set_wait_limit_ns(unsigned long long ns);
 
 /*
  * attn_set_test_stall - test hook for the failure path. While `on` is nonzero,
- * every launch's MMA-issuing thread first waits on a barrier that nothing
- * signals; the wait runs out after the wait limit, the kernel drains and
+ * every attn_fwd launch's MMA-issuing threads, and the S/dV-issuing thread of
+ * every attn_bwd launch, first wait on a barrier that nothing signals; the wait runs out after the wait limit, the kernel drains and
  * returns, and attn_device_status reports ATTN_ERR_TIMEOUT. No fault, trap or
  * hang is involved. Process-wide; off by default.
  */

@@ -59,3 +59,34 @@ def test_wait_timeout_is_reported_and_context_survives(d, causal):
     assert bos.attn_device_status() == bos.ATTN_OK
     o_ref, lse_ref = oracle.attention(qh, kh, vh, float(np.float32(0.1)), causal)
     assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "after timeout")
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_backward_wait_timeout_is_reported_and_context_survives(d, causal):
+    """The same hook on attn_bwd: its S/dV issuer waits on a barrier nothing
+    signals, every role gives up after the limit (the other MMA thread, the
+    producer and the dQ warps with work in flight drain it first), the status
+    reads ATTN_ERR_TIMEOUT, and the next backward is correct."""
+    qh, kh, vh = make_qkv(1, 4, 700, d, seed=23)
+    gh = torch.randn(qh.shape, generator=torch.Generator().manual_seed(24)).to(torch.bfloat16)
+    q, k, v, g = (t.cuda() for t in (qh, kh, vh, gh))
+    scale = float(np.float32(d ** -0.5))
+    o, lse = bos.attention(q, k, v, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert bos.attn_device_status() == bos.ATTN_OK
+    bos.attn_set_wait_limit_ns(20_000_000)          # 20 ms
+    bos.attn_set_test_stall(True)
+    try:
+        bos.attention_backward(q, k, v, o, lse, g, scale=scale, causal=causal)
+        status = bos.attn_device_status()
+    finally:
+        bos.attn_set_test_stall(False)
+        bos.attn_set_wait_limit_ns(0)
+    assert status == bos.ATTN_ERR_TIMEOUT
+    assert bos.attn_device_status() == bos.ATTN_OK
+    grads = bos.attention_backward(q, k, v, o, lse, g, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert bos.attn_device_status() == bos.ATTN_OK
+    for name, gpu, ref in zip(("dq", "dk", "dv"), grads, oracle.attention_bwd(qh, kh, vh, gh, scale, causal)):
+        err = np.abs(gpu.float().cpu().numpy() - ref).max()
+        assert err <= 2e-2 * np.abs(ref).max() + 1e-3, f"{name}: {err}"
