@@ -29,16 +29,19 @@ std::mutex g_device_mu;
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Checks that need no GPU. Returns ATTN_OK or the first failing status.
+// max_d: the widest head dim the caller's kernels take (forward 256, backward 128).
 int validate_host(const void* q, const void* k, const void* v, const void* o, const void* lse,
-                  int B, int H, int N, int d, float scale, int causal, bool device_ptrs) {
+                  int B, int H, int N, int d, float scale, int causal, bool device_ptrs, int max_d = 256) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULLPTR;
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_BAD_SHAPE;
     const int64_t rows = (int64_t)B * H * N;
-    const int64_t units = (int64_t)B * H * ((N + 255) / 256);   // 256-row work units
+    // work units: 256 query rows (d <= 128) or 128 (d > 128)
+    const int64_t unit_rows = d > 128 ? 128 : 256;
+    const int64_t units = (int64_t)B * H * ((N + unit_rows - 1) / unit_rows);
     if ((int64_t)B * H > INT_MAX || rows > ((int64_t)1 << 40) || units > INT_MAX / 2)
         return ATTN_ERR_BAD_SHAPE;
-    // a multiple of 8 (rows of Q, K, V, O must be 16-byte strided for TMA) up to 128
-    if (d < 8 || d > 128 || d % 8 != 0) return ATTN_ERR_UNSUPPORTED_D;
+    // a multiple of 8 (rows of Q, K, V, O must be 16-byte strided for TMA) up to max_d
+    if (d < 8 || d > max_d || d % 8 != 0) return ATTN_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return ATTN_ERR_BAD_SCALE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_ARG;
     if (device_ptrs) {
@@ -161,8 +164,8 @@ extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, 
 
 extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
     static const char one = 0;
-    if (validate_host(&one, &one, &one, &one, reinterpret_cast<const float*>(&one), B, H, N, d, 1.0f, 0, false) !=
-        ATTN_OK)
+    if (validate_host(&one, &one, &one, &one, reinterpret_cast<const float*>(&one), B, H, N, d, 1.0f, 0, false,
+                      128) != ATTN_OK)
         return 0;
     return bos::attn_bwd_workspace(B, H, N, d);
 }
@@ -170,7 +173,7 @@ extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                         const float* lse, const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                         int B, int H, int N, int d, float scale, int causal, void* stream) {
-    int st = validate_host(q, k, v, dq, lse, B, H, N, d, scale, causal, true);
+    int st = validate_host(q, k, v, dq, lse, B, H, N, d, scale, causal, true, 128);
     if (st != ATTN_OK) return st;
     if (!o || !dout || !dk || !dv || !workspace) return ATTN_ERR_NULLPTR;
     if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256) ||
@@ -224,7 +227,8 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_NULLPTR: return "a required pointer is NULL";
         case ATTN_ERR_BAD_SHAPE: return "B, H and N must be >= 1 and the sizes must fit the index space";
-        case ATTN_ERR_UNSUPPORTED_D: return "head dimension d must be a multiple of 8 from 8 to 128";
+        case ATTN_ERR_UNSUPPORTED_D:
+            return "head dimension d must be a multiple of 8 from 8 to 256 (to 128 for the backward)";
         case ATTN_ERR_BAD_SCALE: return "scale must be finite";
         case ATTN_ERR_MISALIGNED: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";
         case ATTN_ERR_UNSUPPORTED_DEVICE: return "the current device is not compute capability 10.3 (sm_103a)";

@@ -118,6 +118,7 @@ struct Cfg {
 
 struct KernelArgs {
     int BH, H, N, U, causal;
+    int d;   // the caller's head dim (the kernel's width may be larger)
     float scale_log2;
     __nv_bfloat16* o;
     float* lse;
@@ -794,6 +795,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 }  // namespace bos
 
 #include "attn_fwd_d64.cuh"
+#include "attn_fwd_d256.cuh"
 
 namespace bos {
 namespace {
@@ -841,18 +843,23 @@ std::atomic<unsigned int> g_sched_next{0};
 
 template <int D>
 int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
-    constexpr int kSmemBytes = (D == 64) ? d64::Cfg::kSmemBytes : Cfg<128>::kSmemBytes;
-    auto* const kernel = (D == 64) ? attn_fwd_d64_kernel : attn_fwd_sm103_kernel<128>;
+    constexpr int kSmemBytes =
+        (D == 64) ? d64::Cfg::kSmemBytes : (D == 256) ? d256::Cfg::kSmemBytes : Cfg<128>::kSmemBytes;
+    auto* const kernel =
+        (D == 64) ? attn_fwd_d64_kernel : (D == 256) ? attn_fwd_d256_kernel : attn_fwd_sm103_kernel<128>;
+    // rows per work unit: two 128-row Q tiles, or one for d > 128
+    constexpr int kRowsPerUnit = (D == 256) ? kBM : kUnitRows;
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return ATTN_ERR_CUDA;
     const int BH = p.B * p.H;
     CUtensorMap mq, mk, mv, mo;
-    // Q, K and V move in 128-row boxes; O is stored 32 rows (one warp) at a time
+    // Q, K and V move in 128-row boxes (V in 64-row key halves for d > 128); O is
+    // stored 32 rows (one warp) at a time
     // (the maps describe the caller's d columns; boxes are 64 wide, so columns
     // from d up to the kernel's width D load as zero and are not stored)
     if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, p.sq, kBM) ||
         !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, p.sk, kBN) ||
-        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, p.sv, kBN) ||
+        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, p.sv, D == 256 ? kBN / 2 : kBN) ||
         !encode_qkv_map(enc, &mo, p.o, p.B, p.H, p.N, p.d, p.so, 32))
         return ATTN_ERR_BAD_SHAPE;
     static int sms_cache[64] = {0};
@@ -887,8 +894,9 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.BH = BH;
     a.H = p.H;
     a.N = p.N;
-    a.U = (p.N + kUnitRows - 1) / kUnitRows;
+    a.U = (p.N + kRowsPerUnit - 1) / kRowsPerUnit;
     a.causal = p.causal;
+    a.d = p.d;
     a.scale_log2 = (float)((double)p.scale * 1.4426950408889634);
     a.o = static_cast<__nv_bfloat16*>(p.o);
     a.lse = p.lse;
@@ -899,7 +907,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     const int grid = (int)(units < sms ? units : sms);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(D == 256 ? d256::kThreads : kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -919,7 +927,9 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
 int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev) {
     // head dims below a kernel's width run on it with the missing columns
     // zero-filled by TMA on load and clipped on store
-    return p.d <= 64 ? launch_d<64>(p, stream, dev) : launch_d<128>(p, stream, dev);
+    if (p.d <= 64) return launch_d<64>(p, stream, dev);
+    if (p.d <= 128) return launch_d<128>(p, stream, dev);
+    return launch_d<256>(p, stream, dev);
 }
 
 void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs; }

@@ -59,7 +59,14 @@ CAUSAL_8K = Workload("causal_b2h16n8192d128", 2, 16, 8192, 128, True, 4)
 TAIL_4000 = Workload("tail_b8h32n4000d64_x4", 8, 32, 4000, 64, False, 5, 4.0)
 
 WORKLOADS = (SMALL, MEDIUM, CAUSAL_2K, CAUSAL_8K, TAIL_4000)
-BY_NAME = {w.name: w for w in WORKLOADS}
+
+# Wider head dims (the page's d = 64 / 128 examples extended to 256 by the same
+# zero-padding reading), measured beside the five above.
+CAUSAL_4K_D256 = Workload("causal_b2h16n4096d256", 2, 16, 4096, 256, True, 6)
+WIDE_2K_D256 = Workload("b4h16n2048d256", 4, 16, 2048, 256, False, 7)
+EXTRA_WORKLOADS = (CAUSAL_4K_D256, WIDE_2K_D256)
+
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int, logit_mult: float = 1.0):

@@ -34,7 +34,7 @@ typedef enum attn_status {
     ATTN_OK = 0,
     ATTN_ERR_NULLPTR = 1,            /* a required pointer is NULL */
     ATTN_ERR_BAD_SHAPE = 2,          /* B, H or N < 1, or the sizes overflow the index space */
-    ATTN_ERR_UNSUPPORTED_D = 3,      /* d is not a multiple of 8 in [8, 128] */
+    ATTN_ERR_UNSUPPORTED_D = 3,      /* d is not a multiple of 8 in [8, 256] ([8, 128] for attn_bwd) */
     ATTN_ERR_BAD_SCALE = 4,          /* scale is NaN or infinite */
     ATTN_ERR_MISALIGNED = 5,         /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
     ATTN_ERR_UNSUPPORTED_DEVICE = 6, /* the current device is not compute capability 10.3 */
@@ -57,11 +57,13 @@ typedef enum attn_status {
  *   B, H, N : batch, heads, sequence length; each >= 1. N need not be a
  *             multiple of any tile size: keys past N do not exist and rows past
  *             N are neither read as outputs nor written.
- *   d       : head dimension, a multiple of 8 from 8 to 128. Kernels exist for
- *             64 and 128 columns; any other d runs on the next one up, the
- *             missing columns read as zero by the tensor copies (they add
+ *   d       : head dimension, a multiple of 8 from 8 to 256. Kernels exist for
+ *             64, 128 and 256 columns; any other d runs on the next one up,
+ *             the missing columns read as zero by the tensor copies (they add
  *             nothing to q . k or to O) and never written, so no padded copy
- *             of the inputs is made.
+ *             of the inputs is made ("Sizing the attention kernel" of "4.4
+ *             Writing GPU Kernels with Triton": zero-padding the head dim is
+ *             exact). The backward, attn_bwd, takes d up to 128.
  *   scale   : the multiplier of q . k (1/sqrt(d) in the pages; a C ABI has no
  *             default, so the caller passes it). Must be finite.
  *   causal  : 0 or 1. With 1, query i attends to keys 0..i.
@@ -91,7 +93,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *       >= d; o must not map two elements to one address.
  *   lse : fp32 [B, H, N], contiguous, as attn_fwd.
  *   other arguments as attn_fwd (pointers 16-byte aligned, d a multiple of 8
- *   up to 128).
+ *   up to 256).
  *
  * Returns the attn_fwd codes; ATTN_ERR_NULLPTR for a NULL stride array,
  * ATTN_ERR_BAD_ARG for strides that break the rules above. attn_fwd itself is

@@ -56,7 +56,8 @@ def _call(lib, q=16, k=32, v=48, o=64, lse=80, B=1, H=1, N=8, d=64, scale=0.125,
     (dict(B=0), bos.ATTN_ERR_BAD_SHAPE), (dict(H=-1), bos.ATTN_ERR_BAD_SHAPE),
     (dict(N=0), bos.ATTN_ERR_BAD_SHAPE), (dict(B=1 << 20, H=1 << 20), bos.ATTN_ERR_BAD_SHAPE),
     (dict(d=60), bos.ATTN_ERR_UNSUPPORTED_D), (dict(d=0), bos.ATTN_ERR_UNSUPPORTED_D),
-    (dict(d=136), bos.ATTN_ERR_UNSUPPORTED_D), (dict(d=4), bos.ATTN_ERR_UNSUPPORTED_D),
+    (dict(d=264), bos.ATTN_ERR_UNSUPPORTED_D), (dict(d=4), bos.ATTN_ERR_UNSUPPORTED_D),
+    (dict(d=260), bos.ATTN_ERR_UNSUPPORTED_D),
     (dict(scale=float("nan")), bos.ATTN_ERR_BAD_SCALE), (dict(scale=float("inf")), bos.ATTN_ERR_BAD_SCALE),
     (dict(causal=2), bos.ATTN_ERR_BAD_ARG),
     (dict(q=17), bos.ATTN_ERR_MISALIGNED), (dict(o=72), bos.ATTN_ERR_MISALIGNED),
@@ -64,6 +65,21 @@ def _call(lib, q=16, k=32, v=48, o=64, lse=80, B=1, H=1, N=8, d=64, scale=0.125,
 ])
 def test_host_validation_before_any_launch(lib, kw, code):
     assert _call(lib, **kw) == code
+
+
+@pytest.mark.parametrize("d", [8, 64, 72, 128, 136, 200, 256])
+def test_head_dims_pass_validation(lib, d):
+    """Every multiple of 8 up to 256 gets past the host checks (here the call
+    then fails only for want of a GPU)."""
+    st = _call(lib, d=d)
+    assert st not in (bos.ATTN_ERR_UNSUPPORTED_D, bos.ATTN_ERR_BAD_ARG, bos.ATTN_ERR_BAD_SHAPE)
+
+
+def test_backward_head_dims_stop_at_128(lib):
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.attn_bwd_workspace_bytes(1, 2, 300, 128) > 0
+    assert lib.attn_bwd_workspace_bytes(1, 2, 300, 136) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 2, 300, 256) == 0
 
 
 def _call_strided(lib, qs=(8 * 64, 8 * 64, 64), os_=(8 * 64, 8 * 64, 64), B=1, H=1, N=8, d=64, null=None):

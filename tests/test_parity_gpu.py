@@ -10,8 +10,8 @@ import torch
 
 import blocked_online_softmax_gb300 as bos
 import oracle
-from blocked_online_softmax_gb300.workloads import (CAUSAL_2K, CAUSAL_8K, MEDIUM, SMALL, TAIL_4000,
-                                                    make_qkv, workload_qkv)
+from blocked_online_softmax_gb300.workloads import (CAUSAL_2K, CAUSAL_4K_D256, CAUSAL_8K, MEDIUM, SMALL,
+                                                    TAIL_4000, WIDE_2K_D256, make_qkv, workload_qkv)
 from parity_util import assert_parity, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -68,7 +68,7 @@ def test_edge_lengths(N, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_several_tiles_ragged_tail(d, causal):
     """Several query/key tiles, odd batch and head counts, a ragged tail."""
     B, H, N = 2, 3, 1000
@@ -90,7 +90,7 @@ def test_other_head_dims(d, causal):
     assert_parity(o, lse, o_ref, lse_ref, f"N=300 d={d} causal={causal}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("mult", [4.0, 8.0])
 @pytest.mark.parametrize("causal", [False, True])
 def test_large_logits_stability(mult, causal, d):
@@ -182,7 +182,8 @@ def test_host_buffer_entry_chunked_matches_device_entry():
 
 # ------------------------------------------------------------------ full-size workloads, sampled
 
-@pytest.mark.parametrize("w", [MEDIUM, CAUSAL_2K, CAUSAL_8K, TAIL_4000], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [MEDIUM, CAUSAL_2K, CAUSAL_8K, TAIL_4000, CAUSAL_4K_D256, WIDE_2K_D256],
+                         ids=lambda w: w.name)
 def test_workload_full_size_sampled(w):
     q, k, v = workload_qkv(w)
     o, lse = run_guarded(q, k, v, w.scale, w.causal)
@@ -218,7 +219,8 @@ def _layout(x, kind, pad=16):
     return base[..., :d], base
 
 
-@pytest.mark.parametrize("d,causal,N", [(128, True, 333), (128, False, 300), (64, True, 257), (40, False, 200)])
+@pytest.mark.parametrize("d,causal,N", [(128, True, 333), (128, False, 300), (64, True, 257), (40, False, 200),
+                                         (256, True, 333), (176, False, 300)])
 @pytest.mark.parametrize("kind", ["bnhd", "padded"])
 def test_strided_layouts(kind, d, causal, N):
     """attn_fwd_strided on [B,N,H,d] views and on rows padded past d, inputs and
@@ -266,7 +268,7 @@ def test_long_sequence_sampled(d, causal, N):
     assert_parity(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, f"N={N} d={d}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_many_short_heads(d):
     """4096 heads of 130 rows: thousands of one- and two-block units through
     the scheduler, each with a ragged tail; compared in full."""
@@ -275,6 +277,33 @@ def test_many_short_heads(d):
     o, lse = run_guarded(q, k, v, scale, True)
     o_ref, lse_ref = oracle.attention(q, k, v, scale, True)
     assert_parity(o, lse, o_ref, lse_ref, f"4096 heads d={d}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [136, 192, 200, 256])
+@pytest.mark.parametrize("N", [1, 127, 129, 300, 600])
+def test_wide_head_dims(N, d, causal):
+    """Head dims past 128 run on the 256-wide kernel: 64-column boxes past d are
+    skipped and the rest of the last box reads as zero."""
+    q, k, v = make_qkv(1, 2, N, d, seed=N + d)
+    scale = float(np.float32(d ** -0.5))
+    o, lse = run_guarded(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    assert_parity(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_causal_mixed_units(d):
+    """Causal, 80 heads of 1900 rows (15 key blocks): about four units per CTA.
+    In every unit but a head's last, the upper 128 query rows see one key block
+    more than the lower 128; the last unit's two tiles see the same blocks. So
+    the tile that takes the upper rows changes from unit to unit in a way that
+    depends on each CTA's sequence of units; every row is compared."""
+    q, k, v = make_qkv(2, 40, 1900, d, seed=97 + d)
+    scale = float(np.float32(d ** -0.5))
+    o, lse = run_guarded(q, k, v, scale, True)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, True)
+    assert_parity(o, lse, o_ref, lse_ref, f"80 heads N=1900 d={d}")
 
 
 def test_concurrent_host_threads():
