@@ -68,14 +68,19 @@ struct Cfg {
 };
 static_assert(Cfg::kSmemBytes <= 232448, "shared memory per CTA");
 
-// Work unit k: 128 query rows. Causal: heaviest first over all heads (as the
-// d <= 128 kernels order their 256-row units); non-causal: head-major.
+// Work unit k: 128 query rows. Causal: heaviest first within each group of
+// heads (as the d <= 128 kernels order their 256-row units); non-causal:
+// head-major.
 __device__ __forceinline__ Unit decode_tile_unit(int k, const KernelArgs& a) {
     Unit u;
     int q;
     if (a.causal) {
-        q = a.U - 1 - k / a.BH;
-        u.bh = k % a.BH;
+        const int gu = a.group * a.U;
+        const int h0 = (k / gu) * a.group;
+        const int gh = min(a.group, a.BH - h0);
+        const int kk = k - (k / gu) * gu;
+        q = a.U - 1 - kk / gh;
+        u.bh = h0 + kk % gh;
     } else {
         u.bh = k / a.U;
         q = k % a.U;

@@ -13,8 +13,9 @@
 //  * Work unit = 256 query rows of one (batch, head) = two 128-row Q tiles that
 //    share every K/V tile. CTAs are persistent (one per SM) and take units from
 //    a per-launch global counter; units are numbered heaviest first (for causal
-//    masking, over all heads), so the triangle of work balances itself and SMs
-//    that run slower simply take fewer units.
+//    masking, within groups of heads whose K and V fit a slice of L2), so the
+//    triangle of work balances itself and SMs that run slower simply take
+//    fewer units.
 //  * Warp roles (384 threads): warpgroups 0 and 1 run the softmax of Q tile 0
 //    and Q tile 1, one thread per query row, with 208 registers each after a
 //    setmaxnreg split; warp 8 takes units and issues TMA loads (Q per unit, then
@@ -118,7 +119,8 @@ struct Cfg {
 
 struct KernelArgs {
     int BH, H, N, U, causal;
-    int d;   // the caller's head dim (the kernel's width may be larger)
+    int d;       // the caller's head dim (the kernel's width may be larger)
+    int group;   // causal: heads per scheduling group (units run heaviest first within a group)
     float scale_log2;
     __nv_bfloat16* o;
     float* lse;
@@ -170,9 +172,13 @@ struct Unit {
 __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
     Unit u;
     int q;
-    if (a.causal) {            // heaviest first over all heads
-        q = a.U - 1 - k / a.BH;
-        u.bh = k % a.BH;
+    if (a.causal) {            // heaviest first within each group of heads
+        const int gu = a.group * a.U;
+        const int h0 = (k / gu) * a.group;
+        const int gh = min(a.group, a.BH - h0);
+        const int kk = k - (k / gu) * gu;
+        q = a.U - 1 - kk / gh;
+        u.bh = h0 + kk % gh;
     } else {                   // head-major (every unit costs the same)
         u.bh = k / a.U;
         q = k % a.U;
@@ -837,6 +843,9 @@ bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int B, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// L2 bytes the K and V of one causal scheduling group of heads may take.
+constexpr double kGroupKvBytes = 32.0 * 1024 * 1024;
+
 uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
 int g_test_stall = 0;
 std::atomic<unsigned int> g_sched_next{0};
@@ -897,6 +906,14 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.U = (p.N + kRowsPerUnit - 1) / kRowsPerUnit;
     a.causal = p.causal;
     a.d = p.d;
+    // Causal units run heaviest first within groups of heads whose K and V
+    // together fit kGroupKvBytes, so the K/V tiles a group re-reads stay in L2
+    // (ordering over every head at once kept all heads' K/V in flight).
+    {
+        const double kv_head = 4.0 * (double)p.N * (double)D;   // bf16 K and V of one head, at the kernel's width
+        const double g = kGroupKvBytes / kv_head;
+        a.group = g >= (double)BH ? BH : (g < 1.0 ? 1 : (int)g);
+    }
     a.scale_log2 = (float)((double)p.scale * 1.4426950408889634);
     a.o = static_cast<__nv_bfloat16*>(p.o);
     a.lse = p.lse;

@@ -39,7 +39,7 @@ def test_status_ok_after_normal_runs():
     assert bos.attn_device_status() == bos.ATTN_OK
 
 
-@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True), (256, True), (192, False)])
 def test_wait_timeout_is_reported_and_context_survives(d, causal):
     qh, kh, vh = make_qkv(2, 8, 1024, d, seed=22)
     q, k, v = (t.cuda() for t in (qh, kh, vh))

@@ -163,6 +163,16 @@ def test_host_buffer_entry():
     assert_parity(o.float().numpy(), lse.numpy(), o_ref, lse_ref, "host entry")
 
 
+def test_host_buffer_entry_wide_head_dim():
+    B, H, N, d = 1, 3, 333, 256
+    q, k, v = make_qkv(B, H, N, d, seed=14)
+    o = torch.empty_like(q).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    bos.attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), o, lse, B, H, N, d, 0.0625, 1)
+    o_ref, lse_ref = oracle.attention(q, k, v, 0.0625, True)
+    assert_parity(o.float().numpy(), lse.numpy(), o_ref, lse_ref, "host entry d=256")
+
+
 def test_host_buffer_entry_chunked_matches_device_entry():
     """Large enough that attn_fwd_host pipelines several chunks of heads over its streams."""
     B, H, N, d = 2, 16, 2048, 128           # 50 MB of inputs -> 3 chunks

@@ -104,3 +104,21 @@ def test_operator_on_transposed_inputs():
         grad = x.grad.permute(0, 2, 1, 3).float().cpu().numpy()
         err = np.abs(grad - r).max()
         assert err <= 2e-2 * np.abs(r).max() + 1e-3, f"{name}: {err}"
+
+
+@pytest.mark.gpu
+def test_wide_head_dim_forward_and_backward_limit():
+    """d = 256 runs forward through the operator; its backward reports the
+    backward's head-dim limit (128) instead of computing anything."""
+    import oracle
+    import blocked_online_softmax_gb300 as bos
+    from blocked_online_softmax_gb300.workloads import make_qkv
+    from parity_util import assert_parity
+    qh, kh, vh = make_qkv(1, 2, 200, 256, seed=88)
+    q, k, v = (t.cuda().requires_grad_(True) for t in (qh, kh, vh))
+    o, lse = torch.ops.bos.attention_fwd(q, k, v, 0.0625, True)
+    o_ref, lse_ref = oracle.attention(qh, kh, vh, 0.0625, True)
+    assert_parity(o.detach().float().cpu().numpy(), lse.detach().cpu().numpy(), o_ref, lse_ref, "op d=256")
+    with pytest.raises(bos.AttnError) as ei:
+        o.float().sum().backward()
+    assert ei.value.status == bos.ATTN_ERR_UNSUPPORTED_D
