@@ -208,9 +208,9 @@ int attn_abi_version(void);
  *   workspace        : device memory of workspace_bytes >=
  *                      attn_bwd_workspace_bytes(B, H, N, d), 256-byte aligned:
  *                      the fp32 dq accumulator (every key block adds its part
- *                      with atomic adds) and the fp32 row sums D. Owned by the
- *                      caller; nothing is allocated.
- *   B, H, N, d, scale, causal, stream: as attn_fwd.
+ *                      with bulk tensor reductions) and the fp32 row sums D.
+ *                      Owned by the caller; nothing is allocated.
+ *   B, H, N, d, scale, causal, stream: as attn_fwd, with d up to 128.
  *
  * Asynchronous on stream. Returns the attn_fwd validation codes, or
  * ATTN_ERR_BAD_ARG when the workspace is smaller than needed; on an error
