@@ -20,16 +20,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_one_sync() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n .reg .b32 rx;\n .reg .pred px;\n"
-        " elect.sync rx|px, 0xffffffff;\n"
-        " selp.b32 %0, 1, 0, px;\n}\n"
-        : "=r"(pred));
-    return pred;
-}
-
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -227,16 +217,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
         "tcgen05.wait::ld.sync.aligned;\n"
         : BOS_R8(0), BOS_R8(8), BOS_R8(16), BOS_R8(24)
-        : "r"(taddr)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : BOS_R8(0), BOS_R8(8)
         : "r"(taddr)
         : "memory");
 }
