@@ -265,7 +265,7 @@ def test_strided_matches_contiguous_bitwise():
 
 # ------------------------------------------------------------------ scale and concurrency
 
-@pytest.mark.parametrize("d,causal,N", [(128, True, 65536), (64, False, 40000)])
+@pytest.mark.parametrize("d,causal,N", [(128, True, 65536), (64, False, 40000), (256, True, 32768), (192, False, 20000)])
 def test_long_sequence_sampled(d, causal, N):
     """One long sequence (index arithmetic at scale, 256-512 work units in one
     head): sampled rows against the oracle, every row finite."""
