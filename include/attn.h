@@ -73,6 +73,10 @@ typedef enum attn_status {
  * first; on any error it returns a nonzero status and launches nothing and
  * writes nothing. On success the kernel is enqueued on `stream` and the call
  * returns without synchronising. Safe to call from several host threads.
+ * May be captured in a CUDA graph (it allocates nothing and only enqueues
+ * work on `stream`). Each launch draws a slot of work counters, and a
+ * captured launch keeps its slot, so one graph instance must not be replayed
+ * on two streams at the same time.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int N, int d, float scale, int causal, void* stream);
