@@ -37,7 +37,7 @@ ATTN_ERR_TOO_LARGE = 11
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
                     "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version",
-                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided")
+                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided", "attn_fwd_ex")
 
 _lib = None
 
@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, vp]
     lib.attn_fwd_strided.restype = i
     lib.attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp, vp, vp, vp, f, i, vp]
+    lib.attn_fwd_ex.restype = i
+    lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp, vp, vp, vp, f, i, i, vp]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     _lib = lib
@@ -140,6 +142,27 @@ def attn_fwd_strided(q, k, v, o, lse, B: int, H: int, N: int, d: int, q_strides,
                                          _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_strided")
+
+
+ATTN_DTYPE_BF16 = 0
+ATTN_DTYPE_F16 = 1
+
+
+def attn_fwd_ex(q, k, v, o, lse, B: int, H: int, N: int, d: int, q_strides, k_strides, v_strides, o_strides,
+                scale: float, causal, dtype: int, stream=None) -> None:
+    """Enqueue the forward kernel for bf16 or fp16 tensors (C ``attn_fwd_ex``).
+
+    ``dtype`` is ATTN_DTYPE_BF16 or ATTN_DTYPE_F16; each ``*_strides`` is three
+    element strides (batch, head, row) or None for a dense tensor. Raises
+    AttnError on a nonzero status.
+    """
+    arrs = [None if st is None else (ctypes.c_longlong * 3)(*[int(x) for x in st])
+            for st in (q_strides, k_strides, v_strides, o_strides)]
+    ptrs = [None if a is None else ctypes.addressof(a) for a in arrs]
+    st = load_library().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                                    *ptrs, float(scale), int(causal), int(dtype), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_ex")
 
 
 def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B: int, H: int, N: int, d: int, scale: float,
@@ -239,7 +262,7 @@ def softmax(x, out=None, stream=None):
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=None, out=None):
-    """O, LSE for bf16 CUDA tensors [B,H,N,d]; scale defaults to 1/sqrt(d) rounded to fp32.
+    """O, LSE for bf16 or fp16 CUDA tensors [B,H,N,d]; scale defaults to 1/sqrt(d) rounded to fp32.
 
     q, k, v (and ``out``, an optional preallocated O) may be strided views, e.g.
     [B,N,H,d] tensors transposed to [B,H,N,d], as long as the head dim is
@@ -249,17 +272,25 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False, stream=
     import torch
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
         raise ValueError("q, k, v must be [B,H,N,d] with one shape")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bf16 or fp16 CUDA tensors")
     for t in (q, k, v):
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise ValueError("q, k, v must be bf16 CUDA tensors")
+        if t.dtype != q.dtype or not t.is_cuda:
+            raise ValueError("q, k, v must be CUDA tensors of one dtype (bf16 or fp16)")
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q, memory_format=torch.contiguous_format) if out is None else out
-    if o.shape != q.shape or o.dtype != torch.bfloat16:
-        raise ValueError("out must be a bf16 tensor shaped like q")
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("out must be a tensor shaped like q, of q's dtype")
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if all(t.is_contiguous() for t in (q, k, v, o)):
+    if q.dtype == torch.float16:
+        for t in (q, k, v, o):
+            if t.stride(3) != 1:
+                raise ValueError("the head dim (last) of q, k, v and out must be contiguous")
+        attn_fwd_ex(q, k, v, o, lse, B, H, N, d, *[t.stride()[:3] for t in (q, k, v, o)], scale, causal,
+                    ATTN_DTYPE_F16, stream)
+    elif all(t.is_contiguous() for t in (q, k, v, o)):
         attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
     else:
         for t in (q, k, v, o):

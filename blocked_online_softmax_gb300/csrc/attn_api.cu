@@ -119,10 +119,12 @@ bool non_overlapping(const long long* s, int B, int H, int N, int d) {
 
 }  // namespace
 
-extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                                int N, int d, const long long* q_strides, const long long* k_strides,
-                                const long long* v_strides, const long long* o_strides, float scale, int causal,
-                                void* stream) {
+namespace {
+
+// attn_fwd_strided's body, for either element type (f16: fp16, else bf16).
+int fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                const long long* q_strides, const long long* k_strides, const long long* v_strides,
+                const long long* o_strides, float scale, int causal, int f16, void* stream) {
     int st = validate_host(q, k, v, o, lse, B, H, N, d, scale, causal, true);
     if (st != ATTN_OK) return st;
     if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_NULLPTR;
@@ -137,6 +139,7 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     p.B = B; p.H = H; p.N = N; p.d = d;
     p.scale = scale; p.causal = causal;
+    p.f16 = f16;
     for (int i = 0; i < 3; ++i) {
         p.sq[i] = q_strides[i];
         p.sk[i] = k_strides[i];
@@ -144,6 +147,28 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
         p.so[i] = o_strides[i];
     }
     return bos::launch_attn_fwd(p, static_cast<cudaStream_t>(stream), dev);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int N, int d, const long long* q_strides, const long long* k_strides,
+                                const long long* v_strides, const long long* o_strides, float scale, int causal,
+                                void* stream) {
+    return fwd_strided(q, k, v, o, lse, B, H, N, d, q_strides, k_strides, v_strides, o_strides, scale, causal, 0,
+                       stream);
+}
+
+extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                           int d, const long long* q_strides, const long long* k_strides,
+                           const long long* v_strides, const long long* o_strides, float scale, int causal,
+                           int dtype, void* stream) {
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F16) return ATTN_ERR_BAD_ARG;
+    // a NULL stride array means that tensor is dense [B, H, N, d]
+    const long long dense[3] = {(long long)H * N * d, (long long)N * d, (long long)d};
+    return fwd_strided(q, k, v, o, lse, B, H, N, d, q_strides ? q_strides : dense, k_strides ? k_strides : dense,
+                       v_strides ? v_strides : dense, o_strides ? o_strides : dense, scale, causal,
+                       dtype == ATTN_DTYPE_F16 ? 1 : 0, stream);
 }
 
 extern "C" int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,

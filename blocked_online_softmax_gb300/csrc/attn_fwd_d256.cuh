@@ -173,9 +173,10 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
 // Part of S(g) = Q K^T into the accumulator at `d_tmem`: the 16-column steps of
 // head-dimension boxes box0 .. box1-1, Q from its buffer, K from the half-tile
 // slot `sKh` that holds those boxes. The first half starts the accumulation.
+template <bool kF16>
 __device__ __forceinline__ void issue_s_half(uint32_t d_tmem, const uint8_t* sQ, const uint8_t* sKh, int box0,
                                              int box1, bool first_half) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, false, kF16);
     const uint32_t qa = smem_u32(sQ), ka = smem_u32(sKh);
 #pragma unroll 1
     for (int bx = box0; bx < box1; ++bx) {
@@ -204,6 +205,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t tm, uint32_t sbuf, const 
 // The MMA stream, one thread: for each unit S(0), S(1), PV(0), S(2), PV(1), ...,
 // PV(n-1), with the CTA's blocks numbered g = 0, 1, ... across units (S(g) in
 // buffer g % 2).
+template <bool kF16>
 __device__ void mma_issuer(uint32_t tm, const uint8_t* sQ, const uint8_t* sKV, uint64_t* bars, const UnitRing& ring,
                            volatile int* abort_flag, const KernelArgs& a) {
     uint64_t* kv_full = bars + kBarKV;
@@ -211,7 +213,7 @@ __device__ void mma_issuer(uint32_t tm, const uint8_t* sQ, const uint8_t* sKV, u
     const uint64_t lim = a.wait_limit_ns;
     const int total = a.BH * a.U;
     const int nb = head_boxes(a);
-    const uint32_t idesc_pv = idesc_bf16_f32(kBM, 64 * nb, false, true);
+    const uint32_t idesc_pv = idesc_f32acc(kBM, 64 * nb, false, true, kF16);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t s_count = 0;    // S blocks issued so far (g of the next S)
@@ -237,9 +239,9 @@ __device__ void mma_issuer(uint32_t tm, const uint8_t* sQ, const uint8_t* sKV, u
                 if (i + 1 == 0 && !wait_or_abort(&bars[kBarQFull], r & 1, lim, abort_flag)) { ok = false; break; }
                 const uint32_t sbuf = (s_count & 1) * kTmemSBuf;
                 tc_fence_after();
-                issue_s_half(tm + sbuf, sQ, sKV + k0 * Cfg::kSlotBytes, 0, min(2, nb), true);
+                issue_s_half<kF16>(tm + sbuf, sQ, sKV + k0 * Cfg::kSlotBytes, 0, min(2, nb), true);
                 mma_commit(&kv_empty[k0]);
-                issue_s_half(tm + sbuf, sQ, sKV + k1 * Cfg::kSlotBytes, 2, nb, false);
+                issue_s_half<kF16>(tm + sbuf, sQ, sKV + k1 * Cfg::kSlotBytes, 2, nb, false);
                 mma_commit(&kv_empty[k1]);
                 mma_commit(&bars[kBarSFull + (s_count & 1)]);
                 if (i + 1 == u.n - 1) mma_commit(&bars[kBarQEmpty]);
@@ -270,6 +272,7 @@ __device__ void mma_issuer(uint32_t tm, const uint8_t* sQ, const uint8_t* sKV, u
 // phases behind the PV barrier), rescale O when the max moved, hand P(g) to
 // the stream. After a unit's last block: O / l as bf16, one 64-column slice at
 // a time, through two 4 KB staging buffers per warp and TMA; LSE.
+template <bool kF16>
 __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, const UnitRing& ring,
                              volatile int* abort_flag, uint8_t* sEpi, const CUtensorMap* tm_o, const KernelArgs& a) {
     const uint64_t lim = a.wait_limit_ns;
@@ -330,7 +333,7 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {   // all 128 keys as bf16 pairs over the buffer's first 64 columns
                 uint32_t pk[16];
-                exp_pack(sr, ch, c2, negm2, acc, pk);
+                exp_pack<kF16>(sr, ch, c2, negm2, acc, pk);
                 tmem_st16(tS + ch * 16, pk);
             }
             if (g > 0 && !wait_warp(&bars[kBarPvDone], (g - 1) & 1)) { ok = false; break; }
@@ -373,10 +376,10 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
             for (int q = 0; q < 8; ++q) {   // 16-byte chunk = 8 output columns
                 const uint32_t* ov = (q < 4) ? o0 + q * 8 : o1 + (q - 4) * 8;
                 uint4 w;
-                w.x = pack_bf16(__uint_as_float(ov[0]) * inv, __uint_as_float(ov[1]) * inv);
-                w.y = pack_bf16(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv);
-                w.z = pack_bf16(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv);
-                w.w = pack_bf16(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv);
+                w.x = pack2<kF16>(__uint_as_float(ov[0]) * inv, __uint_as_float(ov[1]) * inv);
+                w.y = pack2<kF16>(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv);
+                w.z = pack2<kF16>(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv);
+                w.w = pack2<kF16>(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv);
                 *reinterpret_cast<uint4*>(erow + ((q ^ swz) << 4)) = w;
             }
             fence_proxy_async_smem();
@@ -415,6 +418,7 @@ __device__ void init_barriers(uint64_t* bars) {
 
 }  // namespace d256
 
+template <bool kF16>
 __global__ void __launch_bounds__(d256::kThreads, 1)
 attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -456,12 +460,12 @@ attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < d256::kWarpProducer) {
-        d256::softmax_role(tmem, warp, lane, bars, ring, abort_flag, sEpi, &tm_o, a);
+        d256::softmax_role<kF16>(tmem, warp, lane, bars, ring, abort_flag, sEpi, &tm_o, a);
     } else if (warp == d256::kWarpProducer) {
         if (lane == 0) d256::producer(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, a);
         __syncwarp();
     } else {
-        if (lane == 0) d256::mma_issuer(tmem, sQ, sKV, bars, ring, abort_flag, a);
+        if (lane == 0) d256::mma_issuer<kF16>(tmem, sQ, sKV, bars, ring, abort_flag, a);
         __syncwarp();
     }
 

@@ -107,8 +107,9 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
 }
 
 // S_t = Q_t K^T (K = 64: four steps of 16 within one 128-byte swizzled row).
+template <bool kF16>
 __device__ __forceinline__ void issue_s(uint32_t tm, const uint8_t* sQt, const uint8_t* sK) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, false, kF16);
     const uint32_t qa = smem_u32(sQt), ka = smem_u32(sK);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
@@ -117,8 +118,9 @@ __device__ __forceinline__ void issue_s(uint32_t tm, const uint8_t* sQt, const u
 }
 
 // O_t (+)= P_t[:, keys 64h .. 64h+63] * V[those keys, :], P from its tensor-memory columns.
+template <bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t tm, const uint8_t* sV, int h, bool accumulate) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kD, false, true);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, kD, false, true, kF16);
     const uint32_t va = smem_u32(sV);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {   // 16 keys per step: 8 P columns, 16 V rows (2048 bytes)
@@ -128,6 +130,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tm, const uint8_t* sV, int h, 
     }
 }
 
+template <bool kF16>
 __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sKV, uint64_t* bars,
                            const UnitRing& ring, volatile int* abort_flag, const KernelArgs& a) {
     uint64_t* kv_full = bars + kBarKV;
@@ -172,7 +175,7 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
                         break;
                     }
                     tc_fence_after();
-                    issue_s(tm, sQt, sKV + kst * Cfg::kTileBytes);
+                    issue_s<kF16>(tm, sQt, sKV + kst * Cfg::kTileBytes);
                     mma_commit(s_full);
                     ++s_count;
                 }
@@ -186,11 +189,11 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
                 const uint32_t par = pv_count & 1;
                 if (!wait_or_abort(p_half, par, lim, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                issue_pv(tm, sKV + vst * Cfg::kTileBytes, 0, i > first);
+                issue_pv<kF16>(tm, sKV + vst * Cfg::kTileBytes, 0, i > first);
                 mma_commit(pa_done);
                 if (!wait_or_abort(p_full, par, lim, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                issue_pv(tm, sKV + vst * Cfg::kTileBytes, 1, true);
+                issue_pv<kF16>(tm, sKV + vst * Cfg::kTileBytes, 1, true);
                 mma_commit(pb_done);
                 ++pv_count;
             }
@@ -202,16 +205,18 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
 }
 
 // Keys 64h .. 64h+63 of P_t (chunks 2h and 2h+1) into P_t's tensor-memory columns.
+template <bool kF16>
 __device__ __forceinline__ void p_half_to_tmem(const uint32_t (&sr)[128], int h, uint64_t c2, uint64_t negm2,
                                                uint64_t (&acc)[4], uint32_t tP) {
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
-        exp_pack(sr, 2 * h + cc, c2, negm2, acc, pk);
+        exp_pack<kF16>(sr, 2 * h + cc, c2, negm2, acc, pk);
         tmem_st16(tP + (2 * h + cc) * 16, pk);
     }
 }
 
+template <bool kF16>
 __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, const UnitRing& ring,
                              volatile int* abort_flag, uint8_t* sEpi, const CUtensorMap* tm_o, const KernelArgs& a) {
     uint64_t* s_full = bars + kBarSFull + t;
@@ -287,7 +292,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             if (prev && !wait_warp(pa_done, par)) { ok = false; break; }
             tc_fence_after();
-            p_half_to_tmem(sr, 0, c2, negm2, acc, tP);
+            p_half_to_tmem<kF16>(sr, 0, c2, negm2, acc, tP);
             // Rescale O_t after the first half of the exponentials, so the wait for
             // the previous block's PV overlaps them; it must land before PV(i).
             bool pb_seen = false;
@@ -309,7 +314,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             mbar_arrive(p_half);
             if (prev && !pb_seen && !wait_warp(pb_done, par)) { ok = false; break; }
             tc_fence_after();
-            p_half_to_tmem(sr, 1, c2, negm2, acc, tP);
+            p_half_to_tmem<kF16>(sr, 1, c2, negm2, acc, tP);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full);
@@ -337,10 +342,10 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         for (int q = 0; q < 8; ++q) {     // 16-byte chunk = 8 output columns
             const int col = q * 8;
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
+            w.x = pack2<kF16>(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
+            w.y = pack2<kF16>(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
+            w.z = pack2<kF16>(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
+            w.w = pack2<kF16>(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
             *reinterpret_cast<uint4*>(erow + ((q ^ swz) << 4)) = w;
         }
         fence_proxy_async_smem();
@@ -382,6 +387,7 @@ __device__ void init_barriers(uint64_t* bars) {
 
 }  // namespace d64
 
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -424,7 +430,7 @@ attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     if (warp < kWarpProducer) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-        d64::softmax_role(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, ring, abort_flag, sEpi, &tm_o, a);
+        d64::softmax_role<kF16>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, ring, abort_flag, sEpi, &tm_o, a);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
@@ -432,7 +438,7 @@ attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             __syncwarp();
         } else if (warp == kWarpMma0 || warp == kWarpMma1) {
             const int t = warp - kWarpMma0;
-            if (lane == 0) d64::mma_issuer(t ? tmem1 : tmem0, t, sQ, sKV, bars, ring, abort_flag, a);
+            if (lane == 0) d64::mma_issuer<kF16>(t ? tmem1 : tmem0, t, sQ, sKV, bars, ring, abort_flag, a);
             __syncwarp();
         }
     }

@@ -42,6 +42,7 @@
 //    drains its own copies and MMAs, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -227,6 +228,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Two values rounded to the forward's element type (bf16, or fp16 with kF16),
+// lo in the low half.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (kF16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        return pack_bf16(lo, hi);
+    }
+}
+
 // ------------------------------------------------------------------ roles
 
 template <int D>
@@ -290,9 +303,9 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
 }
 
 // S_t = Q_t K^T into the tile's TMEM allocation `tm`.
-template <int D>
+template <int D, bool kF16>
 __device__ __forceinline__ void issue_s(uint32_t tm, const uint8_t* sQt, const uint8_t* sK) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, false, kF16);
     const uint32_t qa = smem_u32(sQt), ka = smem_u32(sK);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -304,9 +317,9 @@ __device__ __forceinline__ void issue_s(uint32_t tm, const uint8_t* sQt, const u
 
 // O_t (+)= P_t[:, keys 0-63] * V[keys 0-63, :], P from tensor memory (packed
 // bf16 pairs over the first 32 columns of S_t).
-template <int D>
+template <int D, bool kF16>
 __device__ __forceinline__ void issue_pv_lo(uint32_t tm, const uint8_t* sV, bool accumulate) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, D, false, true, kF16);
     const uint32_t va = smem_u32(sV);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)       // 16 keys per step: 8 P columns, 16 V rows (2048 bytes)
@@ -316,9 +329,9 @@ __device__ __forceinline__ void issue_pv_lo(uint32_t tm, const uint8_t* sV, bool
 
 // O_t += P_t[:, keys 64-127] * V[keys 64-127, :], P from shared memory
 // (K-major, 128-byte swizzle, one 128-byte row per query).
-template <int D>
+template <int D, bool kF16>
 __device__ __forceinline__ void issue_pv_hi(uint32_t tm, const uint8_t* sPbt, const uint8_t* sV) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, D, false, true, kF16);
     const uint32_t pa = smem_u32(sPbt), va = smem_u32(sV);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
@@ -336,7 +349,7 @@ __device__ __forceinline__ void issue_pv_hi(uint32_t tm, const uint8_t* sPbt, co
 // scores while the softmax is still writing the second half of P.
 // Both streams walk the same K/V ring (K_j, V_j alternating); a stage is free
 // once both have committed it.
-template <int D>
+template <int D, bool kF16>
 __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t* sPb, const uint8_t* sKV,
                            uint64_t* bars, const UnitRing& ring, volatile int* abort_flag, const KernelArgs& a) {
     using C = Cfg<D>;
@@ -367,7 +380,7 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
             if (!wait_or_abort(p_full, pf_phase, lim, abort_flag)) return false;
             pf_phase ^= 1;
             tc_fence_after();
-            issue_pv_hi<D>(tm, sPbt, sKV + vst * C::kTileBytes);
+            issue_pv_hi<D, kF16>(tm, sPbt, sKV + vst * C::kTileBytes);
             mma_commit(pb_done);
         }
         mma_commit(&kv_empty[vst]);
@@ -388,7 +401,7 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
             if (!next_stage(kst)) { ok = false; break; }
             if (active) {
                 tc_fence_after();
-                issue_s<D>(tm, sQt, sKV + kst * C::kTileBytes);
+                issue_s<D, kF16>(tm, sQt, sKV + kst * C::kTileBytes);
                 mma_commit(s_full);
             }
             mma_commit(&kv_empty[kst]);
@@ -399,7 +412,7 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
                 if (!wait_or_abort(p_half, ph_phase, lim, abort_flag)) { ok = false; break; }
                 ph_phase ^= 1;
                 tc_fence_after();
-                issue_pv_lo<D>(tm, sKV + vst * C::kTileBytes, i > first);
+                issue_pv_lo<D, kF16>(tm, sKV + vst * C::kTileBytes, i > first);
             }
             vprev = vst;
         }
@@ -493,6 +506,7 @@ __device__ __forceinline__ void mask_row(uint32_t (&sr)[128], float c, int lim) 
 // pair, p = 2^x (masked columns hold the raw value whose x is -inf, see
 // mask_row), packed into 16 bf16 pairs (key 2e in the low half of pk[e]); the
 // fp32 probabilities are added pairwise into acc[4].
+template <bool kF16>
 __device__ __forceinline__ void exp_pack(const uint32_t (&sr)[128], int ch, uint64_t c2, uint64_t negm2,
                                          uint64_t (&acc)[4], uint32_t (&pk)[16]) {
 #pragma unroll
@@ -503,29 +517,31 @@ __device__ __forceinline__ void exp_pack(const uint32_t (&sr)[128], int ch, uint
         f2_unpack(x2, x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
         acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-        pk[e] = pack_bf16(p0, p1);
+        pk[e] = pack2<kF16>(p0, p1);
     }
 }
 
 // Keys 0-63 of P_t: chunks 0 and 1 into tensor memory (over S_t's first 32 columns).
+template <bool kF16>
 __device__ __forceinline__ void p_lo_to_tmem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
                                              uint64_t (&acc)[4], uint32_t tS) {
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         uint32_t pk[16];
-        exp_pack(sr, ch, c2, negm2, acc, pk);
+        exp_pack<kF16>(sr, ch, c2, negm2, acc, pk);
         tmem_st16(tS + ch * 16, pk);
     }
 }
 
 // Keys 64-127 of P_t: chunks 2 and 3 into this row of the shared-memory half,
 // K-major with the 128-byte swizzle (16-byte chunk q of the row at q ^ (row & 7)).
+template <bool kF16>
 __device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
                                              uint64_t (&acc)[4], uint8_t* prow, int swz) {
 #pragma unroll
     for (int ch = 2; ch < 4; ++ch) {
         uint32_t pk[16];
-        exp_pack(sr, ch, c2, negm2, acc, pk);
+        exp_pack<kF16>(sr, ch, c2, negm2, acc, pk);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int c16 = (ch - 2) * 4 + q;
@@ -541,7 +557,7 @@ __device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t
 // is done) in the 128-byte-swizzled layout. Each warp stores its own 32 rows
 // with TMA (rows past N are clipped), so the epilogue needs no barrier wider
 // than a warp.
-template <int D>
+template <int D, bool kF16>
 __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bars, const UnitRing& ring,
                              volatile int* abort_flag, uint8_t* sPb, const CUtensorMap* tm_o, const KernelArgs& a) {
     using C = Cfg<D>;
@@ -616,7 +632,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             // keys 0-63 into tensor memory; the MMA takes them (and then computes the
             // next block's scores) while keys 64-127 are being exponentiated
-            p_lo_to_tmem(sr, c2, negm2, acc, tS);
+            p_lo_to_tmem<kF16>(sr, c2, negm2, acc, tS);
             // Rescale O_t after the first half of the exponentials, so the wait for
             // the previous block's PV_hi overlaps them; it must land before PV_lo(i).
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -647,7 +663,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 __syncwarp();
                 store_pending = false;
             }
-            p_hi_to_smem(sr, c2, negm2, acc, prow, swz);
+            p_hi_to_smem<kF16>(sr, c2, negm2, acc, prow, swz);
             fence_proxy_async_smem();
             mbar_arrive(p_full);
             const uint64_t s01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
@@ -678,10 +694,10 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             for (int q = 0; q < 8; ++q) {     // 16-byte chunk = 8 output columns
                 const uint32_t* ov = (q < 4) ? o0 + q * 8 : o1 + (q - 4) * 8;
                 uint4 w;
-                w.x = pack_bf16(__uint_as_float(ov[0]) * inv, __uint_as_float(ov[1]) * inv);
-                w.y = pack_bf16(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv);
-                w.z = pack_bf16(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv);
-                w.w = pack_bf16(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv);
+                w.x = pack2<kF16>(__uint_as_float(ov[0]) * inv, __uint_as_float(ov[1]) * inv);
+                w.y = pack2<kF16>(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv);
+                w.z = pack2<kF16>(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv);
+                w.w = pack2<kF16>(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv);
                 *reinterpret_cast<uint4*>(prow + ((q ^ swz) << 4)) = w;
             }
             fence_proxy_async_smem();
@@ -702,7 +718,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
 // ------------------------------------------------------------------ kernel
 
 // Instantiated for D = 128 only; head dims up to 64 run on attn_fwd_d64_kernel.
-template <int D>
+// kF16: Q, K, V, O (and P on the tensor cores) are fp16 instead of bf16.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -767,7 +784,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
     if (warp < kWarpProducer) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-        softmax_role<D>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, ring, abort_flag, sPb, &tm_o, a);
+        softmax_role<D, kF16>(warp < 4 ? tmem0 : tmem1, warp / 4, warp % 4, lane, bars, ring, abort_flag, sPb, &tm_o, a);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
@@ -775,7 +792,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             __syncwarp();
         } else if (warp == kWarpMma0 || warp == kWarpMma1) {
             const int t = warp - kWarpMma0;
-            if (lane == 0) mma_issuer<D>(t ? tmem1 : tmem0, t, sQ, sPb, sKV, bars, ring, abort_flag, a);
+            if (lane == 0) mma_issuer<D, kF16>(t ? tmem1 : tmem0, t, sQ, sPb, sKV, bars, ring, abort_flag, a);
             __syncwarp();
         }
     }
@@ -828,17 +845,18 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// bf16 [B, H, N, d] with element strides st = {batch, head, row} (d
-// contiguous) viewed as a 4-D tensor (column, row, head, batch); boxes of 64
-// columns x `rows` rows, 128-byte swizzle; loads read rows past N (and columns
-// past d) as zero, stores drop them.
+// bf16 (fp16 with f16) [B, H, N, d] with element strides st = {batch, head,
+// row} (d contiguous) viewed as a 4-D tensor (column, row, head, batch); boxes
+// of 64 columns x `rows` rows, 128-byte swizzle; loads read rows past N (and
+// columns past d) as zero, stores drop them.
 bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int B, int H, int N, int d,
-                    const long long (&st)[3], int rows) {
+                    const long long (&st)[3], int rows, bool f16 = false) {
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
     cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
     cuuint32_t elem[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, elem,
+    return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void*>(base), dims, strides, box, elem,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -850,12 +868,13 @@ uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
 int g_test_stall = 0;
 std::atomic<unsigned int> g_sched_next{0};
 
-template <int D>
+template <int D, bool kF16>
 int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     constexpr int kSmemBytes =
         (D == 64) ? d64::Cfg::kSmemBytes : (D == 256) ? d256::Cfg::kSmemBytes : Cfg<128>::kSmemBytes;
-    auto* const kernel =
-        (D == 64) ? attn_fwd_d64_kernel : (D == 256) ? attn_fwd_d256_kernel : attn_fwd_sm103_kernel<128>;
+    auto* const kernel = (D == 64) ? attn_fwd_d64_kernel<kF16>
+                         : (D == 256) ? attn_fwd_d256_kernel<kF16>
+                                      : attn_fwd_sm103_kernel<128, kF16>;
     // rows per work unit: two 128-row Q tiles, or one for d > 128
     constexpr int kRowsPerUnit = (D == 256) ? kBM : kUnitRows;
     EncodeTiledFn enc = get_encode_fn();
@@ -866,10 +885,10 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     // stored 32 rows (one warp) at a time
     // (the maps describe the caller's d columns; boxes are 64 wide, so columns
     // from d up to the kernel's width D load as zero and are not stored)
-    if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, p.sq, kBM) ||
-        !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, p.sk, kBN) ||
-        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, p.sv, D == 256 ? kBN / 2 : kBN) ||
-        !encode_qkv_map(enc, &mo, p.o, p.B, p.H, p.N, p.d, p.so, 32))
+    if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, p.sq, kBM, kF16) ||
+        !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, p.sk, kBN, kF16) ||
+        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, p.sv, D == 256 ? kBN / 2 : kBN, kF16) ||
+        !encode_qkv_map(enc, &mo, p.o, p.B, p.H, p.N, p.d, p.so, 32, kF16))
         return ATTN_ERR_BAD_SHAPE;
     static int sms_cache[64] = {0};
     static int attr_done[64] = {0};
@@ -944,9 +963,14 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
 int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev) {
     // head dims below a kernel's width run on it with the missing columns
     // zero-filled by TMA on load and clipped on store
-    if (p.d <= 64) return launch_d<64>(p, stream, dev);
-    if (p.d <= 128) return launch_d<128>(p, stream, dev);
-    return launch_d<256>(p, stream, dev);
+    if (p.f16) {
+        if (p.d <= 64) return launch_d<64, true>(p, stream, dev);
+        if (p.d <= 128) return launch_d<128, true>(p, stream, dev);
+        return launch_d<256, true>(p, stream, dev);
+    }
+    if (p.d <= 64) return launch_d<64, false>(p, stream, dev);
+    if (p.d <= 128) return launch_d<128, false>(p, stream, dev);
+    return launch_d<256, false>(p, stream, dev);
 }
 
 void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs; }

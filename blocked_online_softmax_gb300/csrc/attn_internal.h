@@ -17,6 +17,7 @@ struct AttnParams {
     int B, H, N, d;
     float scale;
     int causal;
+    int f16 = 0;   // q, k, v, o are fp16 (else bf16)
     // element strides of the batch, head and row dims of q, k, v, o (the head
     // dim is contiguous); set_contiguous fills the dense [B, H, N, d] ones
     long long sq[3], sk[3], sv[3], so[3];

@@ -148,13 +148,18 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // ------------------------------------------------------------------ tcgen05: descriptors
 
-// Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulate.
-// Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format
-// (1 = bf16), 15 A major (1 = MN-major), 16 B major, [17,23) N >> 3,
+// Instruction descriptor for kind::f16 with fp32 accumulate; A and B are both
+// bf16 or both fp16 (one MMA never mixes them).
+// Bits: [4,6) D format (1 = f32), [7,10) A format (0 = f16, 1 = bf16), [10,13)
+// B format (same codes), 15 A major (1 = MN-major), 16 B major, [17,23) N >> 3,
 // [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
            ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_f32acc(M, N, a_mn_major, b_mn_major, false);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.

@@ -69,14 +69,14 @@ EXTRA_WORKLOADS = (CAUSAL_4K_D256, WIDE_2K_D256)
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
-def make_qkv(B: int, H: int, N: int, d: int, seed: int, logit_mult: float = 1.0):
-    """Seeded bf16 Q, K, V on the CPU, contiguous [B, H, N, d]."""
+def make_qkv(B: int, H: int, N: int, d: int, seed: int, logit_mult: float = 1.0, dtype=torch.bfloat16):
+    """Seeded Q, K, V on the CPU, contiguous [B, H, N, d], bf16 (or ``dtype``, e.g. fp16)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     out = []
     for _ in range(3):
         x = torch.randn((B, H, N, d), dtype=torch.float32, generator=g)
-        out.append(x.to(torch.bfloat16))
+        out.append(x.to(dtype))
     q, k, v = out
     if logit_mult != 1.0:
         q = q * logit_mult

@@ -107,6 +107,24 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
                      const long long* q_strides, const long long* k_strides, const long long* v_strides,
                      const long long* o_strides, float scale, int causal, void* stream);
 
+/* Element types of q, k, v and o for attn_fwd_ex. */
+typedef enum attn_dtype {
+    ATTN_DTYPE_BF16 = 0,   /* bfloat16: the type of attn_fwd */
+    ATTN_DTYPE_F16 = 1     /* IEEE half: the pages' examples call the kernel on fp16 tensors */
+} attn_dtype;
+
+/*
+ * attn_fwd_ex - attn_fwd for either element type, with optional strides.
+ * dtype is ATTN_DTYPE_BF16 or ATTN_DTYPE_F16. q, k, v and o share it, and P
+ * enters the second product in it as well; accumulation is fp32 and lse is
+ * fp32 either way. Each *_strides is a host array of 3 element strides as in
+ * attn_fwd_strided, or NULL for a dense [B, H, N, d] tensor. Returns the
+ * attn_fwd_strided codes, and ATTN_ERR_BAD_ARG for an unknown dtype.
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                const long long* q_strides, const long long* k_strides, const long long* v_strides,
+                const long long* o_strides, float scale, int causal, int dtype, void* stream);
+
 /*
  * attn_fwd_host - the same operation on HOST buffers, end to end.
  *

@@ -123,3 +123,18 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(bos.AttnError) as ei:
         bos.attn_fwd(0, 16, 16, 16, 16, 1, 1, 8, 64, 0.1, 0, stream=0)
     assert ei.value.status == bos.ATTN_ERR_NULLPTR
+
+
+def test_fwd_ex_validation(lib):
+    """attn_fwd_ex: unknown dtype and bad strides are refused on the host; NULL
+    strides mean dense tensors, so a valid call fails only for want of a GPU."""
+    def call(dtype=0, qs=None):
+        arr = None if qs is None else (ctypes.c_longlong * 3)(*qs)
+        ptr = None if arr is None else ctypes.addressof(arr)
+        return lib.attn_fwd_ex(16, 32, 48, 64, 80, 1, 1, 8, 64, ptr, None, None, None, ctypes.c_float(0.125), 0,
+                               dtype, None)
+    assert call(dtype=2) == bos.ATTN_ERR_BAD_ARG
+    assert call(dtype=-1) == bos.ATTN_ERR_BAD_ARG
+    assert call(qs=(512, 512, 60)) == bos.ATTN_ERR_BAD_ARG
+    for dt in (bos.ATTN_DTYPE_BF16, bos.ATTN_DTYPE_F16):
+        assert call(dtype=dt) not in (bos.ATTN_ERR_BAD_ARG, bos.ATTN_ERR_NULLPTR, bos.ATTN_ERR_MISALIGNED)
