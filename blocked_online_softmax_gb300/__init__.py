@@ -37,7 +37,7 @@ ATTN_ERR_TOO_LARGE = 11
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
                     "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version",
-                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided", "attn_fwd_ex")
+                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided", "attn_fwd_ex", "attn_bwd_ex")
 
 _lib = None
 
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp, vp, vp, vp, f, i, vp]
     lib.attn_fwd_ex.restype = i
     lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp, vp, vp, vp, f, i, i, vp]
+    lib.attn_bwd_ex.restype = i
+    lib.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, i, vp]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     _lib = lib
@@ -223,12 +225,15 @@ def attn_bwd(q, k, v, o, dout, lse, dlse, dq, dk, dv, workspace, workspace_bytes
 
 def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, stream=None,
                        dlse=None):
-    """dq, dk, dv (bf16) for the attention() forward outputs o, lse and the gradients dout (and dlse, optional)."""
+    """dq, dk, dv (q's dtype: bf16 or fp16) for the attention() forward outputs o, lse and the gradients
+    dout (and dlse, optional)."""
     import torch
     B, H, N, d = q.shape
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v, o, dout must be bf16 or fp16")
     for t in (q, k, v, o, dout):
-        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("q, k, v, o, dout must be contiguous bf16 tensors of one [B,H,N,d] shape")
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous tensors of one dtype and one [B,H,N,d] shape")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     nbytes = attn_bwd_workspace_bytes(B, H, N, d)
@@ -237,7 +242,14 @@ def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal
     if dlse is not None:
         if dlse.dtype != torch.float32 or not dlse.is_contiguous() or tuple(dlse.shape) != (B, H, N):
             raise ValueError("dlse must be a contiguous fp32 [B,H,N] tensor")
-    attn_bwd(q, k, v, o, dout, lse, dlse, dq, dk, dv, ws, nbytes, B, H, N, d, scale, causal, stream)
+    if q.dtype == torch.float16:
+        st = load_library().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dlse),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(nbytes), int(B), int(H), int(N),
+                                        int(d), float(scale), int(causal), ATTN_DTYPE_F16, _stream_handle(stream))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_bwd_ex")
+    else:
+        attn_bwd(q, k, v, o, dout, lse, dlse, dq, dk, dv, ws, nbytes, B, H, N, d, scale, causal, stream)
     return dq, dk, dv
 
 

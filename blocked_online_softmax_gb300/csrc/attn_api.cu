@@ -195,9 +195,12 @@ extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
     return bos::attn_bwd_workspace(B, H, N, d);
 }
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                        const float* lse, const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                        int B, int H, int N, int d, float scale, int causal, void* stream) {
+namespace {
+
+// attn_bwd's body, for either element type (f16: fp16, else bf16).
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H,
+             int N, int d, float scale, int causal, int f16, void* stream) {
     int st = validate_host(q, k, v, dq, lse, B, H, N, d, scale, causal, true, 128);
     if (st != ATTN_OK) return st;
     if (!o || !dout || !dk || !dv || !workspace) return ATTN_ERR_NULLPTR;
@@ -213,7 +216,26 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.dq = dq; p.dk = dk; p.dv = dv; p.workspace = workspace;
     p.B = B; p.H = H; p.N = N; p.d = d;
     p.scale = scale; p.causal = causal;
+    p.f16 = f16;
     return bos::launch_attn_bwd(p, static_cast<cudaStream_t>(stream), dev);
+}
+
+}  // namespace
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, const float* dlse, void* dq, void* dk, void* dv, void* workspace,
+                        size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, void* stream) {
+    return bwd_impl(q, k, v, o, dout, lse, dlse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                    0, stream);
+}
+
+extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                           const float* lse, const float* dlse, void* dq, void* dk, void* dv, void* workspace,
+                           size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, int dtype,
+                           void* stream) {
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F16) return ATTN_ERR_BAD_ARG;
+    return bwd_impl(q, k, v, o, dout, lse, dlse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                    dtype == ATTN_DTYPE_F16 ? 1 : 0, stream);
 }
 
 extern "C" int softmax_rows_fwd(const float* x, float* y, int rows, int cols, long long x_row_stride,

@@ -106,7 +106,7 @@ struct BwdArgs {
     const float* lse;                 // [BH, N] natural log, from the forward pass
     const float* dsum;                // [BH, N] D = rowsum(dO * O) - dLSE
     float* dq_acc;                    // [BH, N, d] fp32, zeroed before the launch
-    __nv_bfloat16* dk;
+    __nv_bfloat16* dk;                // 2-byte elements: bf16, or fp16 in the fp16 build
     __nv_bfloat16* dv;
     uint64_t wait_limit_ns;
     int test_stall;                   // test hook: X first waits on a barrier nothing signals
@@ -130,6 +130,19 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// The two values of a packed pair of the element type (bf16, or fp16 with kF16).
+template <bool kF16>
+__device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
+    if constexpr (kF16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+        lo = f.x;
+        hi = f.y;
+    } else {
+        lo = bf16_lo(v);
+        hi = bf16_hi(v);
+    }
+}
 
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
@@ -169,16 +182,16 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
 }
 
 // X: S^T = K Q_i^T, then dV_j += P^T dO_i once P^T is written.
-template <int D>
+template <int D, bool kF16>
 __device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* abort_flag, int nq,
                       const BwdArgs& a) {
     using C = Cfg<D>;
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t sK = smem_u32(smem + C::kOffK);
     // M = 128 keys, N = 128 queries, K = d; both operands K-major
-    constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t id_s = idesc_f32acc(128, 128, false, false, kF16);
     // M = 128 keys, N = d, K = 128 queries; A from tensor memory, B (dO) N-major
-    constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t id_kv = idesc_f32acc(128, D, false, true, kF16);
     bool ok = !(a.test_stall && !wait_or_abort(&bars[kBarNever], 0, lim, abort_flag)) &&
               wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
     const uint32_t sDO = smem_u32(smem + C::kOffDO);
@@ -210,7 +223,7 @@ __device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* 
 }
 
 // Y: dP^T = V dO_i^T, then dK_j += dS^T Q_i and dQ_i = dS K_j once dS is written.
-template <int D>
+template <int D, bool kF16>
 __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* abort_flag, int nq,
                       const BwdArgs& a) {
     using C = Cfg<D>;
@@ -218,10 +231,10 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
     const uint32_t sDS = smem_u32(smem + C::kOffDS);
-    constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t id_s = idesc_f32acc(128, 128, false, false, kF16);
+    constexpr uint32_t id_kv = idesc_f32acc(128, D, false, true, kF16);
     // M = 128 queries, N = d, K = 128 keys; A (dS) K-major, B (K_j) N-major
-    constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t id_q = idesc_f32acc(128, D, false, true, kF16);
     bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
     const uint32_t sDO = smem_u32(smem + C::kOffDO);
     for (int it = 0; ok && it < nq; ++it) {
@@ -268,7 +281,7 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
 
 // P^T of one block into tensor memory (over the S^T columns already read) and
 // into registers as bf16 pairs (queries 2e, 2e+1 of each 32-query chunk).
-template <bool kMasked>
+template <bool kMasked, bool kF16>
 __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c2x2, int r, bool key_ok, bool diag,
                                         uint32_t (&pk)[64]) {
 #pragma unroll
@@ -287,14 +300,14 @@ __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c
                 if (!key_ok || (diag && qc < r)) p0 = 0.f;
                 if (!key_ok || (diag && qc + 1 < r)) p1 = 0.f;
             }
-            t[e] = pack_bf16(p0, p1);
+            t[e] = pack2<kF16>(p0, p1);
             pk[ch * 16 + e] = t[e];
         }
         tmem_st16(lx + ch * 16, t);
     }
 }
 
-template <int D>
+template <int D, bool kF16>
 __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* bars,
                              volatile int* abort_flag, int bh, int j, int nq, const BwdArgs& a) {
     using C = Cfg<D>;
@@ -329,9 +342,9 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
         const bool diag = a.causal && it == 0;               // the first query block is block j itself
         uint32_t pk[64];
         if (diag || tail_block)
-            p_phase<true>(lx, L, c2x2, r, key_ok, diag, pk);
+            p_phase<true, kF16>(lx, L, c2x2, r, key_ok, diag, pk);
         else
-            p_phase<false>(lx, L, c2x2, r, key_ok, diag, pk);
+            p_phase<false, kF16>(lx, L, c2x2, r, key_ok, diag, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kBarPReady]);
@@ -350,9 +363,10 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
                 const uint32_t p = pk[ch * 16 + e];
                 const uint64_t t2 =
                     f2_fma(f2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), scale2, nd);
-                float ds0, ds1;
-                f2_unpack(f2_mul(f2_pack(bf16_lo(p), bf16_hi(p)), t2), ds0, ds1);
-                dk[e] = pack_bf16(ds0, ds1);
+                float ds0, ds1, p0, p1;
+                unpack2<kF16>(p, p0, p1);
+                f2_unpack(f2_mul(f2_pack(p0, p1), t2), ds0, ds1);
+                dk[e] = pack2<kF16>(ds0, ds1);
             }
             tmem_st16(ly + ch * 16, dk);                      // dS^T over dP^T columns already read
             uint8_t* base = ds_col + ch * 32 * 128;
@@ -393,10 +407,10 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
             for (int e = 0; e < 32; e += 8) {
                 if (c0 + e >= a.d) break;
                 uint4 wv;
-                wv.x = pack_bf16(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-                wv.y = pack_bf16(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                wv.z = pack_bf16(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-                wv.w = pack_bf16(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+                wv.x = pack2<kF16>(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                wv.y = pack2<kF16>(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                wv.z = pack2<kF16>(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+                wv.w = pack2<kF16>(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
                 *reinterpret_cast<uint4*>(dst + c0 + e) = wv;
             }
         }
@@ -480,7 +494,8 @@ __device__ void dq_role(const CUtensorMap* tm_dq, uint32_t tY, int w, int lane, 
 }  // namespace bwd
 
 // One CTA per (key block j, batch*head); heavier key blocks (small j under causal masking) first.
-template <int D>
+// kF16: q, k, v, o, dO and the gradients are fp16 instead of bf16.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
 attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -543,17 +558,17 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const uint32_t tX = tmem_slot[0], tY = tmem_slot[1];
 
     if (warp < bwd::kWarpDq) {
-        bwd::compute_role<D>(tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
+        bwd::compute_role<D, kF16>(tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
     } else if (warp < bwd::kWarpProducer) {
         bwd::dq_role<D>(&tm_dq, tY, warp, lane, smem, bars, abort_flag, bh, i0, nq, a);
     } else if (warp == bwd::kWarpProducer) {
         if (lane == 0) bwd::producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, smem, bars, abort_flag, bh, j, i0, nq, a);
         __syncwarp();
     } else if (warp == bwd::kWarpMmaX) {
-        if (lane == 0) bwd::mma_x<D>(tX, smem, bars, abort_flag, nq, a);
+        if (lane == 0) bwd::mma_x<D, kF16>(tX, smem, bars, abort_flag, nq, a);
         __syncwarp();
     } else {
-        if (lane == 0) bwd::mma_y<D>(tY, smem, bars, abort_flag, nq, a);
+        if (lane == 0) bwd::mma_y<D, kF16>(tY, smem, bars, abort_flag, nq, a);
         __syncwarp();
     }
 
@@ -567,10 +582,11 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 }
 
 // D = rowsum(dO * O) - dLSE in fp32 per row, and the fp32 dQ buffer zeroed.
-// A row is d / 8 lanes (16-byte loads of 8 bf16), so one warp covers
+// A row is d / 8 lanes (16-byte loads of 8 values), so one warp covers
 // 32 / (d / 8) rows at a time (two at d = 128, four at d = 64); grid-stride.
-__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                                                           const __nv_bfloat16* __restrict__ dout,
+template <bool kF16>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                           const uint16_t* __restrict__ dout,
                                                            const float* __restrict__ dlse,
                                                            float* __restrict__ dsum, float* __restrict__ dq_acc,
                                                            int64_t rows, int d) {
@@ -588,8 +604,12 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* 
             const uint4 gv = *reinterpret_cast<const uint4*>(dout + row * d + c);
             const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                s += bwd::bf16_lo(ow[e]) * bwd::bf16_lo(gw[e]) + bwd::bf16_hi(ow[e]) * bwd::bf16_hi(gw[e]);
+            for (int e = 0; e < 4; ++e) {
+                float o0, o1, g0, g1;
+                bwd::unpack2<kF16>(ow[e], o0, o1);
+                bwd::unpack2<kF16>(gw[e], g0, g1);
+                s += o0 * g0 + o1 * g1;
+            }
             float4* z = reinterpret_cast<float4*>(dq_acc + row * d + c);
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -599,25 +619,27 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* 
     }
 }
 
-// dQ: the fp32 accumulation buffer to bf16, eight values per step (n % 8 == 0); grid-stride.
+// dQ: the fp32 accumulation buffer to the element type, eight values per step
+// (n % 8 == 0); grid-stride.
+template <bool kF16>
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restrict__ dq_acc,
-                                                            __nv_bfloat16* __restrict__ dq, int64_t n8) {
+                                                            uint16_t* __restrict__ dq, int64_t n8) {
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const float4 a = __ldcs(reinterpret_cast<const float4*>(dq_acc) + 2 * idx);
         const float4 b = __ldcs(reinterpret_cast<const float4*>(dq_acc) + 2 * idx + 1);
         uint4 w;
-        w.x = pack_bf16(a.x, a.y);
-        w.y = pack_bf16(a.z, a.w);
-        w.z = pack_bf16(b.x, b.y);
-        w.w = pack_bf16(b.z, b.w);
+        w.x = pack2<kF16>(a.x, a.y);
+        w.y = pack2<kF16>(a.z, a.w);
+        w.z = pack2<kF16>(b.x, b.y);
+        w.w = pack2<kF16>(b.z, b.w);
         reinterpret_cast<uint4*>(dq)[idx] = w;
     }
 }
 
 // ------------------------------------------------------------------ host side
 
-template <int D>
+template <int D, bool kF16>
 int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     using C = bwd::Cfg<D>;
     EncodeTiledFn enc = get_encode_fn();
@@ -626,10 +648,10 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     CUtensorMap mq, mk, mv, mdo;
     long long st[3];                                  // dense [B, H, N, d]
     set_strides(st, (long long)p.H * p.N * p.d, (long long)p.N * p.d, p.d);
-    if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, st, 128) ||
-        !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, st, 128) ||
-        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, st, 128) ||
-        !encode_qkv_map(enc, &mdo, p.dout, p.B, p.H, p.N, p.d, st, 128))
+    if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, st, 128, kF16) ||
+        !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, st, 128, kF16) ||
+        !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, st, 128, kF16) ||
+        !encode_qkv_map(enc, &mdo, p.dout, p.B, p.H, p.N, p.d, st, 128, kF16))
         return ATTN_ERR_BAD_SHAPE;
     const int64_t rows = (int64_t)BH * p.N;
     float* dq_acc = static_cast<float*>(p.workspace);
@@ -650,7 +672,7 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     }
     static int attr_done[64] = {0};
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        if (cudaFuncSetAttribute(attn_bwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_bwd_sm103_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_LAUNCH;
@@ -670,9 +692,8 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     const int64_t pre_rows_per_block = 8 * (32 / (p.d <= 8 ? 1 : p.d <= 16 ? 2 : p.d <= 32 ? 4 : p.d <= 64 ? 8 : 16));
     const int64_t pre_need = (rows + pre_rows_per_block - 1) / pre_rows_per_block;
     const int64_t pre_blocks = pre_need < (int64_t)sms * 8 ? pre_need : (int64_t)sms * 8;
-    attn_bwd_pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.dlse, dsum, dq_acc, rows,
-        p.d);
+    attn_bwd_pre_kernel<kF16><<<(unsigned)pre_blocks, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.dlse, dsum, dq_acc, rows, p.d);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     bwd::BwdArgs a;
     a.BH = BH;
@@ -691,13 +712,12 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     a.wait_limit_ns = g_wait_limit_ns;
     a.test_stall = g_test_stall;
     const int64_t grid = (int64_t)BH * a.nkv;
-    attn_bwd_sm103_kernel<D><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+    attn_bwd_sm103_kernel<D, kF16><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     const int64_t n8 = rows * p.d / 8;
     const int64_t post_need = (n8 + 255) / 256;
     const int64_t post_blocks = post_need < (int64_t)sms * 8 ? post_need : (int64_t)sms * 8;
-    attn_bwd_post_kernel<<<(unsigned)post_blocks, 256, 0, stream>>>(
-        dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8);
+    attn_bwd_post_kernel<kF16><<<(unsigned)post_blocks, 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(p.dq), n8);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -710,7 +730,8 @@ size_t attn_bwd_workspace(int B, int H, int N, int d) {
 }
 
 int launch_attn_bwd(const AttnBwdParams& p, cudaStream_t stream, int dev) {
-    return p.d <= 64 ? launch_bwd_d<64>(p, stream, dev) : launch_bwd_d<128>(p, stream, dev);
+    if (p.f16) return p.d <= 64 ? launch_bwd_d<64, true>(p, stream, dev) : launch_bwd_d<128, true>(p, stream, dev);
+    return p.d <= 64 ? launch_bwd_d<64, false>(p, stream, dev) : launch_bwd_d<128, false>(p, stream, dev);
 }
 
 }  // namespace bos

@@ -72,6 +72,7 @@ struct AttnBwdParams {
     int B, H, N, d;
     float scale;
     int causal;
+    int f16 = 0;         // q, k, v, o, dout and the gradients are fp16 (else bf16)
 };
 
 // Bytes of workspace attn_bwd needs (each part 256-byte aligned).

@@ -31,7 +31,7 @@ from . import attention_backward as _attention_backward
 @torch.library.custom_op("bos::attention_fwd", mutates_args=(), device_types="cuda")
 def attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
                   causal: bool) -> tuple[torch.Tensor, torch.Tensor]:
-    """O (bf16 [B,H,N,d]) and LSE (fp32 [B,H,N], natural log) of softmax(scale q k^T [causal]) v."""
+    """O ([B,H,N,d], q's dtype: bf16 or fp16) and LSE (fp32 [B,H,N], natural log) of softmax(scale q k^T [causal]) v."""
     return _attention(q, k, v, scale=scale, causal=causal)
 
 
@@ -47,7 +47,7 @@ def _attention_fwd_fake(q, k, v, scale, causal):
 def attention_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
                   dout: torch.Tensor, dlse: Optional[torch.Tensor], scale: float,
                   causal: bool) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """dq, dk, dv (bf16 [B,H,N,d]) for the forward's o, lse and the gradients dout (and dlse, optional)."""
+    """dq, dk, dv ([B,H,N,d], q's dtype) for the forward's o, lse and the gradients dout (and dlse, optional)."""
     return _attention_backward(q, k, v, o, lse, dout, scale=scale, causal=causal, dlse=dlse)
 
 
@@ -69,7 +69,7 @@ def _backward(ctx, grad_o, grad_lse):
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()   # the backward takes dense [B,H,N,d]
     if grad_o is None:
         grad_o = torch.zeros_like(o)
-    grad_o = grad_o.to(torch.bfloat16).contiguous()
+    grad_o = grad_o.to(q.dtype).contiguous()
     if grad_lse is not None:
         grad_lse = grad_lse.to(torch.float32).contiguous()
     dq, dk, dv = torch.ops.bos.attention_bwd(q, k, v, o, lse, grad_o, grad_lse, ctx.scale, ctx.causal)

@@ -242,6 +242,16 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
              float scale, int causal, void* stream);
 
+/*
+ * attn_bwd_ex - attn_bwd for either element type: dtype is ATTN_DTYPE_BF16 or
+ * ATTN_DTYPE_F16, shared by q, k, v, o, dout, dq, dk and dv (lse, dlse and the
+ * workspace stay fp32). Returns the attn_bwd codes, and ATTN_ERR_BAD_ARG for
+ * an unknown dtype.
+ */
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                const float* dlse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
 /* Workspace bytes attn_bwd needs for these sizes (0 if B, H, N or d are out of range). */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 

@@ -166,7 +166,7 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool, dlse=None):
 
 
 def _to_f64(t):
-    """bf16 torch tensor or array -> float64 numpy array (bf16 widened exactly)."""
+    """bf16 / fp16 torch tensor or array -> float64 numpy array (widened exactly)."""
     if hasattr(t, "dtype") and str(getattr(t, "dtype", "")).endswith("bfloat16"):
         return t.detach().to("cpu").float().numpy().astype(np.float64)
     if hasattr(t, "detach"):

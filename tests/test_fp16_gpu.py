@@ -60,8 +60,31 @@ def test_fp16_operator_forward():
     assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "fp16 operator")
 
 
-def test_fp16_backward_is_refused():
-    q, k, v = (t.cuda() for t in make_qkv(1, 1, 64, 64, seed=680, dtype=torch.float16))
-    o, lse = bos.attention(q, k, v)
-    with pytest.raises(ValueError):
-        bos.attention_backward(q, k, v, o, lse, torch.ones_like(o))
+@pytest.mark.parametrize("d,causal,N", [(64, False, 300), (128, True, 700), (40, True, 129), (128, False, 1000)])
+def test_fp16_backward_against_oracle(d, causal, N):
+    q, k, v = make_qkv(1, 2, N, d, seed=690 + d + N, dtype=torch.float16)
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(691)).to(torch.float16)
+    scale = float(np.float32(d ** -0.5))
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, g))
+    o, lse = bos.attention(qd, kd, vd, scale=scale, causal=causal)
+    grads = bos.attention_backward(qd, kd, vd, o, lse, gd, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    refs = oracle.attention_bwd(q, k, v, g, scale, causal)
+    for name, gpu, ref in zip(("dq", "dk", "dv"), grads, refs):
+        assert gpu.dtype == torch.float16
+        err = float(np.max(np.abs(gpu.float().cpu().numpy() - ref)))
+        bound = 2e-2 * float(np.max(np.abs(ref))) + 1e-3
+        assert err <= bound, f"fp16 {name} d={d} causal={causal} N={N}: {err:.3g} > {bound:.3g}"
+
+
+def test_fp16_autograd_through_operator():
+    import blocked_online_softmax_gb300.torch_op  # noqa: F401
+    q, k, v = make_qkv(1, 2, 300, 64, seed=695, dtype=torch.float16)
+    qd, kd, vd = (t.cuda().requires_grad_(True) for t in (q, k, v))
+    o, lse = torch.ops.bos.attention_fwd(qd, kd, vd, 0.125, True)
+    o.float().sum().backward()
+    g = torch.ones(q.shape, dtype=torch.float16)
+    refs = oracle.attention_bwd(q, k, v, g, 0.125, True)
+    for name, gpu, ref in zip(("dq", "dk", "dv"), (qd.grad, kd.grad, vd.grad), refs):
+        err = float(np.max(np.abs(gpu.float().cpu().numpy() - ref)))
+        assert err <= 2e-2 * float(np.max(np.abs(ref))) + 1e-3, name
