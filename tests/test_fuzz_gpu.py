@@ -1,7 +1,8 @@
 """Seeded randomized parity sweep: shapes, head dims, masks, scales, logit
-sizes and memory layouts drawn at random (fixed seed, so every run checks the
-same cases), each compared in full against the fp64 oracle. The fixed-case
-tests pin the edges; this sweep covers the combinations between them.
+sizes and memory layouts drawn at random (fixed seeds, so every run checks
+the same cases), bf16 and, in a second set, fp16 inputs, each compared in
+full against the fp64 oracle. The fixed-case tests pin the edges; this sweep
+covers the combinations between them.
 
 Tolerance on O. The five measured workloads are held to max|dO| <= 2e-2. Drawn
 cases can have |O| past 4: with x4 logits the softmax is nearly one-hot and
@@ -109,3 +110,38 @@ def test_backward_random_case(case):
         bound = 2e-2 * float(np.max(np.abs(ref))) + 1e-3
         assert err <= bound, (f"case {case} {name}: B={B} H={H} N={N} d={d} causal={causal} scale={scale:g} "
                               f"x{mult:g}: max err {err:.3g} > {bound:.3g}")
+
+
+F16_FWD_CASES = 48
+F16_BWD_CASES = 16
+
+
+def _f16_cases(seed, n, max_d):
+    rng = np.random.default_rng(seed)
+    return [_draw(rng, max_d) for _ in range(n)]
+
+
+@pytest.mark.parametrize("case", range(F16_FWD_CASES))
+def test_forward_random_case_fp16(case):
+    B, H, N, d, causal, scale, mult, layout = _f16_cases(20261204, F16_FWD_CASES, 256)[case]
+    q, k, v = make_qkv(B, H, N, d, seed=4000 + case, logit_mult=mult, dtype=torch.float16)
+    o, lse = bos.attention(_view(q, layout), _view(k, layout), _view(v, layout), scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(q.double(), k.double(), v.double(), scale, causal)
+    what = f"fp16 case {case}: B={B} H={H} N={N} d={d} causal={causal} scale={scale:g} x{mult:g} {layout}"
+    assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, what)
+
+
+@pytest.mark.parametrize("case", range(F16_BWD_CASES))
+def test_backward_random_case_fp16(case):
+    B, H, N, d, causal, scale, mult = _f16_cases(20261205, F16_BWD_CASES, 128)[case][:7]
+    q, k, v = make_qkv(B, H, N, d, seed=5000 + case, logit_mult=mult, dtype=torch.float16)
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(6000 + case)).to(torch.float16)
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, g))
+    o, lse = bos.attention(qd, kd, vd, scale=scale, causal=causal)
+    grads = bos.attention_backward(qd, kd, vd, o, lse, gd, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    for name, gpu, ref in zip(("dq", "dk", "dv"), grads, oracle.attention_bwd(q, k, v, g, scale, causal)):
+        err = float(np.max(np.abs(gpu.float().cpu().numpy() - ref)))
+        bound = 2e-2 * float(np.max(np.abs(ref))) + 1e-3
+        assert err <= bound, f"fp16 case {case} {name}: B={B} H={H} N={N} d={d}: {err:.3g} > {bound:.3g}"
