@@ -98,3 +98,50 @@ def test_uniform_attention_dv_is_mean_of_do():
     k, v, g = rng.standard_normal((3, 1, 1, N, 4))
     _, _, dv = oracle.attention_bwd(q, k, v, g, 1.0, False)
     np.testing.assert_allclose(dv[0, 0], np.broadcast_to(g[0, 0].sum(axis=0) / N, (N, 4)), rtol=1e-13)
+
+
+def _fd_grad_q(q, k, v, g, scale, causal, eps=1e-6):
+    num = np.zeros_like(q)
+    for idx in np.ndindex(q.shape):
+        qp, qm = q.copy(), q.copy()
+        qp[idx] += eps
+        qm[idx] -= eps
+        num[idx] = (_loss(qp, k, v, g, scale, causal) - _loss(qm, k, v, g, scale, causal)) / (2 * eps)
+    return num
+
+
+def _dq_planted(q, k, v, g, scale, mistake):
+    """dq of one non-causal head with one of the page's named backward mistakes
+    planted (the page's failure signatures, "FlashAttention Backward" of "4.4
+    Writing GPU Kernels with Triton"): the D_i term dropped, or the softmax
+    scale folded in wrong (missing from dS)."""
+    s = scale * q @ k.T
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    o = p @ v
+    dp = g @ v.T
+    dsum = (g * o).sum(axis=1, keepdims=True)
+    if mistake == "no_D":
+        ds = p * dp * scale
+    elif mistake == "no_scale":
+        ds = p * (dp - dsum)
+    else:
+        ds = p * (dp - dsum) * scale
+    return ds @ k
+
+
+@pytest.mark.parametrize("mistake", ["no_D", "no_scale"])
+def test_finite_differences_catch_the_pages_backward_mistakes(mistake):
+    """The finite-difference pin is sharp enough to reject each mistake the page
+    names, and accepts the unmutated formula: dropping D adds scale * D_i times
+    row i of P K to dq, and a missing scale multiplies dq by 1/scale."""
+    rng = np.random.default_rng(41)
+    q, k, v, g = (rng.standard_normal((1, 1, 5, 3)) for _ in range(4))
+    scale = 0.6
+    num = _fd_grad_q(q, k, v, g, scale, False)[0, 0]
+    good = _dq_planted(q[0, 0], k[0, 0], v[0, 0], g[0, 0], scale, None)
+    np.testing.assert_allclose(good, num, rtol=1e-6, atol=1e-8)
+    bad = _dq_planted(q[0, 0], k[0, 0], v[0, 0], g[0, 0], scale, mistake)
+    assert np.max(np.abs(bad - num)) > 1e-2 * np.max(np.abs(num)), f"the pin misses the planted {mistake}"
+    if mistake == "no_scale":
+        np.testing.assert_allclose(bad, num / scale, rtol=1e-6, atol=1e-8)
