@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="causal_b2h16n8192d128")
+    ap.add_argument("--dtype", choices=("bf16", "fp16"), default="bf16",
+                    help="element type of q, k, v, o for --op attention (the host-buffer e2e leg is bf16 only)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle sample time")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -296,11 +298,23 @@ def run_ours(args, w):
     _build.build()
     bos.load_library()
 
-    q_h, k_h, v_h = workload_qkv(w)
+    f16 = args.dtype == "fp16"
+    if f16:
+        from blocked_online_softmax_gb300.workloads import make_qkv
+        q_h, k_h, v_h = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.logit_mult, dtype=torch.float16)
+    else:
+        q_h, k_h, v_h = workload_qkv(w)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+
+    def launch():
+        if f16:
+            bos.attn_fwd_ex(q, k, v, o, lse, w.B, w.H, w.N, w.d, None, None, None, None, w.scale, w.causal,
+                            bos.ATTN_DTYPE_F16, stream)
+        else:
+            bos.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
     in_bytes = 3 * q.numel() * 2
     flush = None
     if in_bytes <= 129e6:
@@ -309,7 +323,7 @@ def run_ours(args, w):
     def step():
         if flush is not None:
             flush.zero_()
-        bos.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+        launch()
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -336,7 +350,7 @@ def run_ours(args, w):
             if flush is not None:
                 flush.zero_()
                 starts[i].record(stream)
-            bos.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+            launch()
             if flush is not None:
                 ends[i].record(stream)
         t_end.record(stream)
@@ -357,7 +371,7 @@ def run_ours(args, w):
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e_value, e2e_steps = None, 0
-    if not args.no_e2e:
+    if not args.no_e2e and not f16:
         qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
         op = torch.empty_like(q_h).pin_memory()
         lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
@@ -377,7 +391,7 @@ def run_ours(args, w):
     avg_launch_ms = statistics.fmean(launch_ms)
     achieved = w.flops / (avg_launch_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                "frac": achieved / peak, "traffic": None if f16 else recorded_traffic(w.name),
                 "peak_kind": f"{peaks_kind} dense bf16 burst (cuBLAS)",
                 "kernel": "attn_fwd", "mean_launch_ms": avg_launch_ms,
                 "launch_timing": ("K back-to-back launches between two CUDA events" if flush is None
@@ -387,7 +401,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(w, q_h, k_h, v_h, args.cpu_seconds)
+        cpu = time_oracle(w, *((t.double() if f16 else t) for t in (q_h, k_h, v_h)), args.cpu_seconds)
 
     if dist is not None:
         dist.barrier()
@@ -396,8 +410,8 @@ def run_ours(args, w):
         return 0
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w),
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if f16 else "bf16", "data": "synthetic",
+            "config": dict(workload_config(w), dtype=args.dtype),
             "frac_of_peak": value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
