@@ -8,10 +8,10 @@
 // and every argument is checked before anything is launched.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "attn.h"
 #include "attn_internal.h"
@@ -23,8 +23,7 @@ constexpr int kAbiVersion = 1;
 constexpr int kMaxDevices = 64;
 
 // Per-device cache of the compute-capability check: 0 unknown, 1 ok, 2 unsupported.
-int g_device_ok[kMaxDevices] = {0};
-std::mutex g_device_mu;
+std::atomic<int> g_device_ok[kMaxDevices];
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -56,8 +55,8 @@ int check_device(int* dev_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return ATTN_ERR_CUDA; }
     *dev_out = dev;
-    if (dev >= 0 && dev < kMaxDevices && g_device_ok[dev] != 0)
-        return g_device_ok[dev] == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
+    const int known = (dev >= 0 && dev < kMaxDevices) ? g_device_ok[dev].load(std::memory_order_relaxed) : 0;
+    if (known != 0) return known == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -65,10 +64,7 @@ int check_device(int* dev_out) {
         return ATTN_ERR_CUDA;
     }
     const bool ok = (major == 10 && minor == 3);
-    if (dev >= 0 && dev < kMaxDevices) {
-        std::lock_guard<std::mutex> lk(g_device_mu);
-        g_device_ok[dev] = ok ? 1 : 2;
-    }
+    if (dev >= 0 && dev < kMaxDevices) g_device_ok[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
     return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
 }
 

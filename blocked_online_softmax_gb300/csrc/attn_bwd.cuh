@@ -670,23 +670,24 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return ATTN_ERR_BAD_SHAPE;
     }
-    static int attr_done[64] = {0};
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    // per-device caches, shared by host threads (the values are idempotent)
+    static std::atomic<int> attr_done[64];
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
         if (cudaFuncSetAttribute(attn_bwd_sm103_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_LAUNCH;
         }
-        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+        if (dev >= 0 && dev < 64) attr_done[dev].store(1, std::memory_order_relaxed);
     }
-    static int sms_cache[64] = {0};
-    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+    static std::atomic<int> sms_cache[64];
+    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
     if (sms == 0) {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
-        if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+        if (dev >= 0 && dev < 64) sms_cache[dev].store(sms, std::memory_order_relaxed);
     }
     // the two element-wise passes: grid-stride, 8 blocks of 256 threads per SM
     const int64_t pre_rows_per_block = 8 * (32 / (p.d <= 8 ? 1 : p.d <= 16 ? 2 : p.d <= 32 ? 4 : p.d <= 64 ? 8 : 16));

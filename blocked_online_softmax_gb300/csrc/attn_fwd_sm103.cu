@@ -890,18 +890,19 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
         !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, p.sv, D == 256 ? kBN / 2 : kBN, kF16) ||
         !encode_qkv_map(enc, &mo, p.o, p.B, p.H, p.N, p.d, p.so, 32, kF16))
         return ATTN_ERR_BAD_SHAPE;
-    static int sms_cache[64] = {0};
-    static int attr_done[64] = {0};
-    static unsigned int* sched_cache[64] = {nullptr};
-    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+    // per-device caches, shared by host threads (the values are idempotent)
+    static std::atomic<int> sms_cache[64];
+    static std::atomic<int> attr_done[64];
+    static std::atomic<unsigned int*> sched_cache[64];
+    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
     if (sms == 0) {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
-        if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+        if (dev >= 0 && dev < 64) sms_cache[dev].store(sms, std::memory_order_relaxed);
     }
-    unsigned int* sched = (dev >= 0 && dev < 64) ? sched_cache[dev] : nullptr;
+    unsigned int* sched = (dev >= 0 && dev < 64) ? sched_cache[dev].load(std::memory_order_relaxed) : nullptr;
     if (sched == nullptr) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_attn_sched) != cudaSuccess) {
@@ -909,14 +910,14 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
             return ATTN_ERR_CUDA;
         }
         sched = static_cast<unsigned int*>(ptr);
-        if (dev >= 0 && dev < 64) sched_cache[dev] = sched;
+        if (dev >= 0 && dev < 64) sched_cache[dev].store(sched, std::memory_order_relaxed);
     }
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_LAUNCH;
         }
-        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+        if (dev >= 0 && dev < 64) attr_done[dev].store(1, std::memory_order_relaxed);
     }
     KernelArgs a;
     a.BH = BH;

@@ -24,6 +24,7 @@
 //  * Rows are distributed over a grid-stride loop, so any row count works.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "attn.h"
@@ -179,7 +180,7 @@ softmax_rows_online(const float* __restrict__ x, float* __restrict__ y, int rows
     }
 }
 
-int g_sms[64] = {0};
+std::atomic<int> g_sms[64];   // SM count per device, shared by host threads
 
 template <int G, int K, bool kVec>
 int launch_onchip(const float* x, float* y, int rows, int cols, long long xs, long long ys, cudaStream_t stream,
@@ -207,13 +208,13 @@ int dispatch_k(const float* x, float* y, int rows, int cols, long long xs, long 
 
 int launch_softmax_rows(const float* x, float* y, int rows, int cols, long long xs, long long ys,
                         cudaStream_t stream, int dev) {
-    int sms = (dev >= 0 && dev < 64) ? g_sms[dev] : 0;
+    int sms = (dev >= 0 && dev < 64) ? g_sms[dev].load(std::memory_order_relaxed) : 0;
     if (sms == 0) {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
-        if (dev >= 0 && dev < 64) g_sms[dev] = sms;
+        if (dev >= 0 && dev < 64) g_sms[dev].store(sms, std::memory_order_relaxed);
     }
     if (cols > SOFTMAX_ROWS_ONCHIP_COLS) {
         long long blocks = rows < (long long)sms * 8 ? rows : (long long)sms * 8;
