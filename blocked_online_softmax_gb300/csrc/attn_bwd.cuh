@@ -31,8 +31,11 @@
 // dV and dK products take P^T and dS^T straight from tensor memory.
 // Warps 0-3 (thread = key = lane) form P = exp2(S c - L2) as soon as S^T lands
 // (X can then start dV and the next block's S^T), then dS = P (dP scale -
-// D scale) once dP^T lands; dS also goes to shared memory as [query][key]
-// (128-byte swizzle, K-major), the A operand of the dQ product.
+// D scale) once dP^T lands; dS also goes to shared memory, each thread writing
+// its key's row of 128 queries with 16-byte stores ([key][query], 128-byte
+// swizzle): the A operand of the dQ product, read query-major (MN-major).
+// Scalar stores into a [query][key] layout cost eight times the store
+// instructions on the compute warps' path.
 // Warps 4-7 (thread = query = lane) take the dQ part out of tensor memory,
 // write it to shared memory (an 8 KB slot per warp, 128-byte swizzle) and add
 // it into the fp32 dQ buffer with TMA bulk tensor reductions, so the adds move
@@ -86,7 +89,7 @@ struct Cfg {
     static constexpr int kOffK = 0, kOffV = kTile;
     static constexpr int kOffQ = 2 * kTile;                    // Q stage s at kOffQ + s * kTile
     static constexpr int kOffDO = 4 * kTile;
-    static constexpr int kOffDS = 5 * kTile;                   // dS, [128 queries][128 keys] bf16: 32 KB
+    static constexpr int kOffDS = 5 * kTile;                   // dS, [128 keys][128 queries] bf16: 32 KB
     static constexpr int kOffDQ = kOffDS + 32768;              // dQ staging: 8 KB per dQ warp
     static constexpr int kOffLse = kOffDQ + 32768;             // [2][128] -LSE log2 e, then [2][128] -D scale
     static constexpr int kOffBar = kOffLse + 2048;
@@ -233,8 +236,9 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
     const uint32_t sDS = smem_u32(smem + C::kOffDS);
     constexpr uint32_t id_s = idesc_f32acc(128, 128, false, false, kF16);
     constexpr uint32_t id_kv = idesc_f32acc(128, D, false, true, kF16);
-    // M = 128 queries, N = d, K = 128 keys; A (dS) K-major, B (K_j) N-major
-    constexpr uint32_t id_q = idesc_f32acc(128, D, false, true, kF16);
+    // M = 128 queries, N = d, K = 128 keys; A (dS, stored [key][query]) and
+    // B (K_j, stored [key][d]) both MN-major
+    constexpr uint32_t id_q = idesc_f32acc(128, D, true, true, kF16);
     bool ok = wait_or_abort(&bars[kBarKV], 0, lim, abort_flag);
     const uint32_t sDO = smem_u32(smem + C::kOffDO);
     for (int it = 0; ok && it < nq; ++it) {
@@ -270,8 +274,8 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
             break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)   // 16 keys per step: 32 bytes of each dS row, 16 rows of K_j
-            mma_ss(tY + C::kTdQ, sdesc_sw128(sDS + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+        for (int kk = 0; kk < 8; ++kk)   // 16 keys per step: 16 rows of dS (two 64-query boxes) and of K_j
+            mma_ss(tY + C::kTdQ, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
                    sdesc_sw128(sK + kk * 2048, 16384, 1024), id_q, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarDqReady]);
     }
@@ -316,13 +320,10 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
     const uint32_t lx = tX + ((uint32_t)(w * 32) << 16), ly = tY + ((uint32_t)(w * 32) << 16);
     const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffLse);   // [2][128] -LSE log2 e
     const float* dsc_s = lse_s + 2 * 128;                                      // [2][128] -D scale
-    // this thread's key in the [query][key] dS buffer: box r / 64, 16-byte chunk
-    // (r % 64) / 8 (swizzled with the query row), element r % 8
-    uint8_t* ds_col = smem + C::kOffDS + (r >> 6) * 16384 + (r & 7) * 2;
-    const int ds_chunk = (r & 63) >> 3;
-    uint32_t dsoff[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) dsoff[k] = (uint32_t)((ds_chunk ^ k) << 4);
+    // this thread's row of the [key][query] dS buffer: 128 bytes in each of the two
+    // 64-query boxes, its 16-byte chunks swizzled with the key (r % 8)
+    uint8_t* ds_row = smem + C::kOffDS + r * 128;
+    const int ds_swz = r & 7;
     const uint64_t c2x2 = f2_pack(a.c2, a.c2), scale2 = f2_pack(a.scale, a.scale);
     const int key = j * 128 + r;
     const bool key_ok = key < a.N;
@@ -369,13 +370,11 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
                 dk[e] = pack2<kF16>(ds0, ds1);
             }
             tmem_st16(ly + ch * 16, dk);                      // dS^T over dP^T columns already read
-            uint8_t* base = ds_col + ch * 32 * 128;
+            uint8_t* box = ds_row + (ch >> 1) * 16384;       // queries 32ch..32ch+31: chunks 4(ch&1)..+3
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {                    // dS[query][key r], queries 32ch..32ch+31
-                const uint32_t pair = dk[e >> 1];
-                *reinterpret_cast<uint16_t*>(base + e * 128 + dsoff[e & 7]) =
-                    (uint16_t)((e & 1) ? (pair >> 16) : (pair & 0xffffu));
-            }
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(box + ((((ch & 1) * 4 + c) ^ ds_swz) << 4)) =
+                    make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
             if (ch == 1) {                                    // Y's first four dK steps need only these
                 tmem_st_wait();
                 tc_fence_before();
