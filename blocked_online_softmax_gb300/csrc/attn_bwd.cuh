@@ -109,8 +109,6 @@ struct BwdArgs {
     const float* lse;                 // [BH, N] natural log, from the forward pass
     const float* dsum;                // [BH, N] D = rowsum(dO * O) - dLSE
     float* dq_acc;                    // [BH, N, d] fp32, zeroed before the launch
-    __nv_bfloat16* dk;                // 2-byte elements: bf16, or fp16 in the fp16 build
-    __nv_bfloat16* dv;
     uint64_t wait_limit_ns;
     int test_stall;                   // test hook: X first waits on a barrier nothing signals
 };
@@ -312,7 +310,8 @@ __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c
 }
 
 template <int D, bool kF16>
-__device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t* smem, uint64_t* bars,
+__device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv, uint32_t tX, uint32_t tY, int w,
+                             int lane, uint8_t* smem, uint64_t* bars,
                              volatile int* abort_flag, int bh, int j, int nq, const BwdArgs& a) {
     using C = Cfg<D>;
     const uint64_t lim = a.wait_limit_ns;
@@ -387,33 +386,51 @@ __device__ void compute_role(uint32_t tX, uint32_t tY, int w, int lane, uint8_t*
         mbar_arrive(&bars[kBarDsReady]);
     }
     // dV_j is final once all of X's MMAs are complete, dK_j once all of Y's are.
-    // The tensor-memory loads are warp-collective: every lane takes part, and
-    // only the stores depend on the lane's key being inside the sequence.
-    __nv_bfloat16* dkr = a.dk + ((int64_t)bh * a.N + key) * a.d;
-    __nv_bfloat16* dvr = a.dv + ((int64_t)bh * a.N + key) * a.d;
+    // Each warp converts its 32 keys' rows to the element type, writes them
+    // 128-byte swizzled into a tile no MMA reads any more (dO's for dV: X's dV
+    // products and Y's dP^T, its readers, are complete; V's for dK), and
+    // stores them with TMA, which clips rows past N and columns past d.
+    // Direct 16-byte stores from the lanes touched 32 rows per instruction.
+    const int b_idx = bh / a.H, h_idx = bh % a.H;
+    bool drained = true;
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        if (!wait_warp(&bars[pass == 0 ? kBarDrainX : kBarDrainY], 0)) return;
+    for (int pass = 0; pass < 2 && drained; ++pass) {
+        if (!wait_warp(&bars[pass == 0 ? kBarDrainX : kBarDrainY], 0)) {
+            drained = false;
+            break;
+        }
         tc_fence_after();
         const uint32_t src = (pass == 0 ? lx : ly) + kAcc;
-        __nv_bfloat16* dst = pass == 0 ? dvr : dkr;
+        uint8_t* stage = smem + (pass == 0 ? C::kOffDO : C::kOffV) + w * 4096;   // this warp's 32 rows
+        uint8_t* srow = stage + lane * 128;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(src + c0, v);
-            if (!key_ok) continue;
+        for (int hb = 0; hb < C::kBoxes; ++hb) {     // 64 columns: one 128-byte row per key
+            uint32_t v0[32], v1[32];
+            tmem_ld32(src + hb * 64, v0);
+            tmem_ld32(src + hb * 64 + 32, v1);
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-                if (c0 + e >= a.d) break;
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t* vv = (c < 4) ? v0 + c * 8 : v1 + (c - 4) * 8;
                 uint4 wv;
-                wv.x = pack2<kF16>(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-                wv.y = pack2<kF16>(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                wv.z = pack2<kF16>(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-                wv.w = pack2<kF16>(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
-                *reinterpret_cast<uint4*>(dst + c0 + e) = wv;
+                wv.x = pack2<kF16>(__uint_as_float(vv[0]), __uint_as_float(vv[1]));
+                wv.y = pack2<kF16>(__uint_as_float(vv[2]), __uint_as_float(vv[3]));
+                wv.z = pack2<kF16>(__uint_as_float(vv[4]), __uint_as_float(vv[5]));
+                wv.w = pack2<kF16>(__uint_as_float(vv[6]), __uint_as_float(vv[7]));
+                *reinterpret_cast<uint4*>(srow + hb * 16384 + ((c ^ (lane & 7)) << 4)) = wv;
             }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            for (int hb = 0; hb < C::kBoxes; ++hb)
+                tma_store_4d(pass == 0 ? tm_dv : tm_dk, stage + hb * 16384, hb * 64, j * 128 + w * 32, h_idx, b_idx);
+            bulk_commit();
+        }
+        __syncwarp();
     }
+    // the stores must have read shared memory (and be complete) before the CTA exits
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
 }
 
 // Warps 4-7: stage LSE / D two blocks ahead, read each dQ part out of tensor
@@ -498,7 +515,8 @@ template <int D, bool kF16>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
 attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_dq, const bwd::BwdArgs a) {
+                      const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                      const __grid_constant__ CUtensorMap tm_dv, const bwd::BwdArgs a) {
     using C = bwd::Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw;
@@ -545,6 +563,8 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
         prefetch_tmap(&tm_dq);
+        prefetch_tmap(&tm_dk);
+        prefetch_tmap(&tm_dv);
     }
     if (warp == bwd::kWarpMmaX) {
         tmem_alloc(tmem_slot, bwd::kCols);
@@ -557,7 +577,7 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const uint32_t tX = tmem_slot[0], tY = tmem_slot[1];
 
     if (warp < bwd::kWarpDq) {
-        bwd::compute_role<D, kF16>(tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
+        bwd::compute_role<D, kF16>(&tm_dk, &tm_dv, tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
     } else if (warp < bwd::kWarpProducer) {
         bwd::dq_role<D>(&tm_dq, tY, warp, lane, smem, bars, abort_flag, bh, i0, nq, a);
     } else if (warp == bwd::kWarpProducer) {
@@ -644,13 +664,15 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return ATTN_ERR_CUDA;
     const int BH = p.B * p.H;
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdk, mdv;
     long long st[3];                                  // dense [B, H, N, d]
     set_strides(st, (long long)p.H * p.N * p.d, (long long)p.N * p.d, p.d);
     if (!encode_qkv_map(enc, &mq, p.q, p.B, p.H, p.N, p.d, st, 128, kF16) ||
         !encode_qkv_map(enc, &mk, p.k, p.B, p.H, p.N, p.d, st, 128, kF16) ||
         !encode_qkv_map(enc, &mv, p.v, p.B, p.H, p.N, p.d, st, 128, kF16) ||
-        !encode_qkv_map(enc, &mdo, p.dout, p.B, p.H, p.N, p.d, st, 128, kF16))
+        !encode_qkv_map(enc, &mdo, p.dout, p.B, p.H, p.N, p.d, st, 128, kF16) ||
+        !encode_qkv_map(enc, &mdk, p.dk, p.B, p.H, p.N, p.d, st, 32, kF16) ||   // 32-row boxes: one per warp
+        !encode_qkv_map(enc, &mdv, p.dv, p.B, p.H, p.N, p.d, st, 32, kF16))
         return ATTN_ERR_BAD_SHAPE;
     const int64_t rows = (int64_t)BH * p.N;
     float* dq_acc = static_cast<float*>(p.workspace);
@@ -707,12 +729,10 @@ int launch_bwd_d(const AttnBwdParams& p, cudaStream_t stream, int dev) {
     a.lse = p.lse;
     a.dsum = dsum;
     a.dq_acc = dq_acc;
-    a.dk = static_cast<__nv_bfloat16*>(p.dk);
-    a.dv = static_cast<__nv_bfloat16*>(p.dv);
     a.wait_limit_ns = g_wait_limit_ns;
     a.test_stall = g_test_stall;
     const int64_t grid = (int64_t)BH * a.nkv;
-    attn_bwd_sm103_kernel<D, kF16><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+    attn_bwd_sm103_kernel<D, kF16><<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, mdk, mdv, a);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     const int64_t n8 = rows * p.d / 8;
     const int64_t post_need = (n8 + 255) / 256;
