@@ -12,6 +12,13 @@ Under torchrun each rank runs an independent replica on its own GPU (the work
 units share nothing), so the value is the total FLOPs of all ranks over the
 slowest rank's time ("weak" scaling).
 
+On one GPU the line also carries two records outside the timed region:
+``per_config`` (forward and backward TFLOP/s on each of the five measured
+workloads, each timed by the same rule: L2 flushed before every launch when
+the inputs fit in it, back to back otherwise) and ``sustained`` (the default
+workload back to back for about 1.5 s with the SM clock sampled, reported
+against the measured sustained peak as well).
+
 --impl reference times the fp64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (the pages ship no runnable code; the
 oracle is the reference arm).
@@ -52,6 +59,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle sample time")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload record (every measured workload, forward and backward)")
+    ap.add_argument("--sustained-seconds", type=float, default=1.5,
+                    help="length of the back-to-back sustained leg on the default workload (0 = skip)")
     ap.add_argument("--op", choices=("attention", "softmax", "backward"), default="attention",
                     help="attention (the default hot path), the fused row softmax (a memory-bound workload), "
                          "or the attention backward pass")
@@ -281,6 +292,127 @@ def workload_config(w):
             if in_bytes > 129e6 else "L2 flushed between steps, outside the timed launches"}
 
 
+def time_forward_launches(w, dev, launches, q=None, k=None, v=None):
+    """Mean device time of one forward launch on workload w, by the bench's rule:
+    inputs larger than L2 run back to back between two events; inputs that fit
+    get a 256 MB write before every launch and an event pair around each launch."""
+    import torch
+
+    import blocked_online_softmax_gb300 as bos
+    from blocked_online_softmax_gb300.workloads import workload_qkv
+    if q is None:
+        q, k, v = (t.to(dev) for t in workload_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    in_bytes = 3 * q.numel() * 2
+    flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev) if in_bytes <= 129e6 else None
+    launch = lambda: bos.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            if flush is not None:
+                flush.zero_()
+            launch()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for s_ev, e_ev in ev:
+            if flush is not None:
+                flush.zero_()
+                s_ev.record(stream)
+            launch()
+            if flush is not None:
+                e_ev.record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if flush is not None:
+        ms = statistics.fmean(s_ev.elapsed_time(e_ev) for s_ev, e_ev in ev)
+        mode = "CUDA events around each launch, L2 flushed before each"
+    else:
+        ms = t0.elapsed_time(t1) / launches
+        mode = "back-to-back launches between two CUDA events (inputs larger than L2)"
+    return ms, mode
+
+
+def time_backward_steps(w, dev, steps):
+    """Mean device time of one attn_bwd call (three launches) on workload w, with the
+    forward's timing rule (L2 flushed before each step when the step's inputs fit)."""
+    import torch
+
+    import blocked_online_softmax_gb300 as bos
+    from blocked_online_softmax_gb300.workloads import workload_qkv
+    q_h, k_h, v_h = workload_qkv(w)
+    do_h = torch.randn(q_h.shape, generator=torch.Generator().manual_seed(99)).to(torch.bfloat16)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o, lse = bos.attention(q, k, v, scale=w.scale, causal=w.causal)
+    nbytes = bos.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = 5 * q.numel() * 2
+    flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev) if in_bytes <= 129e6 else None
+    step = lambda: bos.attn_bwd(q, k, v, o, do, lse, None, dq, dk, dv, ws, nbytes, w.B, w.H, w.N, w.d, w.scale,
+                                w.causal, stream)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ev, e_ev in ev:
+        if flush is not None:
+            flush.zero_()
+            s_ev.record(stream)
+        step()
+        if flush is not None:
+            e_ev.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if flush is not None:
+        return statistics.fmean(s_ev.elapsed_time(e_ev) for s_ev, e_ev in ev), \
+            "CUDA events around each step, L2 flushed before each"
+    return t0.elapsed_time(t1) / steps, "back-to-back steps between two CUDA events (inputs larger than L2)"
+
+
+def per_config_record(dev, peak, peak_sus, launches=30, bwd_steps=10):
+    """Forward and backward on every measured workload (the five of the survey's
+    measurement table), each by the bench's timing rule."""
+    from blocked_online_softmax_gb300.workloads import WORKLOADS
+    out = []
+    for w in WORKLOADS:
+        ms, mode = time_forward_launches(w, dev, launches)
+        tf = w.flops / (ms / 1e3) / 1e12
+        rec = {"name": w.name, "workload": w.describe(), "fwd_tflops": tf, "fwd_frac": tf / peak,
+               "fwd_frac_of_sustained": tf / peak_sus, "fwd_mean_launch_ms": ms, "fwd_launches": launches,
+               "fwd_timing": mode}
+        bms, bmode = time_backward_steps(w, dev, bwd_steps)
+        btf = 2.5 * w.flops / (bms / 1e3) / 1e12
+        rec.update({"bwd_tflops": btf, "bwd_frac": btf / peak, "bwd_mean_step_ms": bms,
+                    "bwd_over_fwd_latency": bms / ms, "bwd_steps": bwd_steps, "bwd_timing": bmode,
+                    "bwd_flops_counted": "2.5x the forward's (five N^2 d products)"})
+        out.append(rec)
+    return out
+
+
+def sustained_record(w, dev, seconds, peak, peak_sus, q, k, v):
+    """The default workload back to back for about `seconds`, clocks sampled throughout."""
+    ms_probe, _ = time_forward_launches(w, dev, 5, q, k, v)
+    launches = max(10, int(seconds * 1e3 / max(ms_probe, 1e-3)))
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    sampler.mark()
+    ms, mode = time_forward_launches(w, dev, launches, q, k, v)
+    clocks = sampler.stop()
+    tf = w.flops / (ms / 1e3) / 1e12
+    mhz = clocks.get("sm_mhz")
+    return {"workload": w.name, "launches": launches, "seconds": ms * launches / 1e3, "tflops": tf,
+            "frac": tf / peak, "frac_of_sustained": tf / peak_sus, "mean_launch_ms": ms, "timing": mode,
+            "clocks": clocks,
+            "launch_kcycles_at_median_sm_clock": (ms * mhz) if mhz else None}
+
+
 def run_ours(args, w):
     import torch
 
@@ -403,6 +535,14 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, *((t.double() if f16 else t) for t in (q_h, k_h, v_h)), args.cpu_seconds)
 
+    per_config, sustained = None, None
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    if rank == 0 and world == 1 and not f16:
+        if not args.no_per_config:
+            per_config = per_config_record(dev, peak, peak_sus)
+        if args.sustained_seconds > 0:
+            sustained = sustained_record(w, dev, args.sustained_seconds, peak, peak_sus, q, k, v)
+
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -411,7 +551,7 @@ def run_ours(args, w):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16" if f16 else "bf16", "data": "synthetic",
-            "config": dict(workload_config(w), dtype=args.dtype),
+            "config": workload_config(w),
             "frac_of_peak": value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
@@ -419,7 +559,8 @@ def run_ours(args, w):
                     "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
                     "api": "attn_fwd_host (pinned host buffers; copies, kernel, copies back, sync)"},
             "gpu_launches": args.steps, "clocks": clocks,
-            "kernel_source_sha": kernel_source_hash()}
+            "kernel_source_sha": kernel_source_hash(),
+            "per_config": per_config, "sustained": sustained}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -33,11 +33,13 @@ ATTN_ERR_TIMEOUT = 8
 ATTN_ERR_CUDA = 9
 ATTN_ERR_BAD_ARG = 10
 ATTN_ERR_TOO_LARGE = 11
+ATTN_ERR_SCHED_BUSY = 12
 
 # every symbol include/attn.h declares
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_host", "attn_fwd_host_noalloc", "attn_device_status",
                     "attn_set_wait_limit_ns", "attn_set_test_stall", "attn_status_string", "attn_abi_version",
-                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided", "attn_fwd_ex", "attn_bwd_ex")
+                    "softmax_rows_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_strided", "attn_fwd_ex", "attn_bwd_ex",
+                    "attn_set_test_sched_busy")
 
 _lib = None
 
@@ -68,6 +70,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.attn_set_test_stall.restype = i
     lib.attn_set_test_stall.argtypes = [i]
+    lib.attn_set_test_sched_busy.restype = i
+    lib.attn_set_test_sched_busy.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i]
     lib.attn_abi_version.restype = i
@@ -205,6 +209,11 @@ def attn_set_wait_limit_ns(ns: int) -> None:
 def attn_set_test_stall(on: bool) -> None:
     """Test hook: make every launch's MMA thread wait on a barrier nothing signals."""
     load_library().attn_set_test_stall(int(bool(on)))
+
+
+def attn_set_test_sched_busy(on: bool) -> None:
+    """Test hook: mark each forward launch's work-counter slot as held by another launch."""
+    load_library().attn_set_test_sched_busy(int(bool(on)))
 
 
 def attn_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

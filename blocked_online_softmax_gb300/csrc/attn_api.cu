@@ -265,6 +265,11 @@ extern "C" int attn_set_test_stall(int on) {
     return ATTN_OK;
 }
 
+extern "C" int attn_set_test_sched_busy(int on) {
+    bos::set_test_sched_busy(on);
+    return ATTN_OK;
+}
+
 extern "C" const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
@@ -280,6 +285,9 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_CUDA: return "a CUDA runtime call failed";
         case ATTN_ERR_BAD_ARG: return "malformed argument (causal must be 0 or 1; strides positive multiples of 8, row stride >= d, output not self-overlapping; workspace large enough)";
         case ATTN_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of attn_fwd_host_noalloc (ATTN_NOALLOC_SCRATCH_BYTES)";
+        case ATTN_ERR_SCHED_BUSY:
+            return "a launch found its work-counter slot held by another launch in flight (more than 4096 "
+                   "forward launches outstanding on the device); it skipped its work units";
         default: return "unknown status";
     }
 }

@@ -99,7 +99,7 @@ __device__ __forceinline__ int head_boxes(const KernelArgs& a) { return (a.d + 6
 
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* sQ,
                          uint8_t* sKV, uint64_t* bars, const UnitRing& ring, volatile int* abort_flag,
-                         const KernelArgs& a) {
+                         volatile int* member, const KernelArgs& a) {
     uint64_t* kv_full = bars + kBarKV;
     uint64_t* kv_empty = bars + kBarKV + Cfg::kStages;
     const int total = a.BH * a.U;
@@ -146,7 +146,13 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
             ok = false;
             break;
         }
-        const int k = (r == 0) ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        int k;   // the first unit of CTA g is g; a CTA whose counter slot is held elsewhere takes none
+        if (r == 0) {
+            *member = sched_claim(a.sched) ? 1 : 0;
+            k = *member ? (int)blockIdx.x : total;
+        } else {
+            k = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        }
         ring.idx[sl] = k;
         mbar_arrive(&bars[kBarUnitFull + sl]);
         if (k >= total) break;
@@ -432,6 +438,7 @@ attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    volatile int* member = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 12);   // holds the counter slot
     const UnitRing ring{bars + d256::kBarUnitFull, bars + d256::kBarUnitEmpty,
                         reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -439,6 +446,7 @@ attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (threadIdx.x == 0) {
         d256::init_barriers(bars);
         *abort_flag = 0;
+        *member = 0;
         fence_mbar_init();
     }
     if (warp == d256::kWarpProducer && lane == 0) {
@@ -462,7 +470,7 @@ attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (warp < d256::kWarpProducer) {
         d256::softmax_role<kF16>(tmem, warp, lane, bars, ring, abort_flag, sEpi, &tm_o, a);
     } else if (warp == d256::kWarpProducer) {
-        if (lane == 0) d256::producer(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, a);
+        if (lane == 0) d256::producer(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, member, a);
         __syncwarp();
     } else {
         if (lane == 0) d256::mma_issuer<kF16>(tmem, sQ, sKV, bars, ring, abort_flag, a);
@@ -473,13 +481,7 @@ attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == d256::kWarpMma) tmem_dealloc(tmem, d256::kTmemCols);
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-            atomicExch(a.sched, 0u);
-            atomicExch(a.sched + 1, 0u);
-        }
-    }
+    if (threadIdx.x == 0 && *member) sched_release(a.sched);
 }
 
 }  // namespace

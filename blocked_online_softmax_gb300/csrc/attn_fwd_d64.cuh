@@ -53,7 +53,7 @@ struct Cfg {
 
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* sQ,
                          uint8_t* sKV, uint64_t* bars, const UnitRing& ring, volatile int* abort_flag,
-                         const KernelArgs& a) {
+                         volatile int* member, const KernelArgs& a) {
     uint64_t* kv_full = bars + kBarKV;
     uint64_t* kv_empty = bars + kBarKV + Cfg::kStages;
     const int total = a.BH * a.U;
@@ -78,7 +78,13 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
             ok = false;
             break;
         }
-        const int k = (r == 0) ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        int k;   // the first unit of CTA g is g; a CTA whose counter slot is held elsewhere takes none
+        if (r == 0) {
+            *member = sched_claim(a.sched) ? 1 : 0;
+            k = *member ? (int)blockIdx.x : total;
+        } else {
+            k = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        }
         ring.idx[sl] = k;
         mbar_arrive(&bars[kBarUnitFull + sl]);
         if (k >= total) break;
@@ -401,6 +407,7 @@ attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    volatile int* member = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 12);   // holds the counter slot
     const UnitRing ring{bars + d64::kBarUnitFull, bars + d64::kBarUnitEmpty,
                         reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -408,6 +415,7 @@ attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (threadIdx.x == 0) {
         d64::init_barriers(bars);
         *abort_flag = 0;
+        *member = 0;
         fence_mbar_init();
     }
     if (warp == kWarpProducer && lane == 0) {
@@ -434,7 +442,7 @@ attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
-            if (lane == 0) d64::producer(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, a);
+            if (lane == 0) d64::producer(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, member, a);
             __syncwarp();
         } else if (warp == kWarpMma0 || warp == kWarpMma1) {
             const int t = warp - kWarpMma0;
@@ -450,13 +458,7 @@ attn_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_dealloc(tmem0, kTmemColsPerTile);
         tmem_dealloc(tmem1, kTmemColsPerTile);
     }
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-            atomicExch(a.sched, 0u);
-            atomicExch(a.sched + 1, 0u);
-        }
-    }
+    if (threadIdx.x == 0 && *member) sched_release(a.sched);
 }
 
 }  // namespace

@@ -135,11 +135,16 @@ struct KernelArgs {
 // Sticky device-side status: 0, or the attn_status of the first failure.
 __device__ int g_attn_device_status;
 
-// Work counters, two words per slot: units taken, CTAs finished. Each launch
-// draws the next slot round-robin and its last CTA zeroes the slot again, so a
-// slot is only reused thousands of launches later, long after its kernel ended.
+// Work counters. Each launch draws the next slot round-robin; a slot is four
+// words: units taken, CTAs finished, and the 64-bit tag of the launch that
+// holds it (its %gridid + 1; 0 = free). A CTA claims the slot before it takes
+// a unit; the last CTA out returns the counters to zero and frees the slot. A
+// launch that finds its slot still held by another launch (only possible with
+// more than kSchedSlots launches in flight on the device) takes no units and
+// records ATTN_ERR_SCHED_BUSY instead of sharing the other launch's counter.
 constexpr int kSchedSlots = 4096;
-__device__ unsigned int g_attn_sched[2 * kSchedSlots];
+constexpr int kSchedWords = 4;
+__device__ __align__(16) unsigned int g_attn_sched[kSchedWords * kSchedSlots];
 
 namespace {
 
@@ -162,6 +167,36 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
             atomicCAS(&g_attn_device_status, 0, (int)ATTN_ERR_TIMEOUT);
             return false;
         }
+    }
+}
+
+// The launch's tag in its work-counter slot: unique per launch in this context.
+__device__ __forceinline__ unsigned long long launch_tag() {
+    unsigned long long g;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+    return g + 1ull;
+}
+
+// Claims this launch's counter slot (one thread per CTA, before its first
+// unit). False if another launch still holds it; the status is then recorded.
+__device__ __forceinline__ bool sched_claim(unsigned int* slot) {
+    const unsigned long long me = launch_tag();
+    const unsigned long long held =
+        atomicCAS(reinterpret_cast<unsigned long long*>(slot + 2), 0ull, me);
+    if (held == 0ull || held == me) return true;
+    atomicCAS(&g_attn_device_status, 0, (int)ATTN_ERR_SCHED_BUSY);
+    return false;
+}
+
+// Called once by every CTA that claimed the slot, after all its work: the last
+// one zeroes the counters, then frees the slot for a later launch.
+__device__ __forceinline__ void sched_release(unsigned int* slot) {
+    __threadfence();
+    if (atomicAdd(slot + 1, 1u) == gridDim.x - 1) {
+        atomicExch(slot, 0u);
+        atomicExch(slot + 1, 0u);
+        __threadfence();
+        atomicExch(reinterpret_cast<unsigned long long*>(slot + 2), 0ull);
     }
 }
 
@@ -245,7 +280,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                          uint8_t* sQ, uint8_t* sKV, uint64_t* bars, const UnitRing& ring, volatile int* abort_flag,
-                         const KernelArgs& a) {
+                         volatile int* member, const KernelArgs& a) {
     using C = Cfg<D>;
     uint64_t* kv_full = bars + kBarKV;
     uint64_t* kv_empty = bars + kBarKV + C::kStages;
@@ -275,8 +310,15 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
             break;
         }
         // the first unit of CTA g is g (the grid never exceeds the unit count); the
-        // counter hands out the rest
-        const int k = (r == 0) ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        // counter hands out the rest. A CTA whose slot is held by another launch
+        // takes no unit.
+        int k;
+        if (r == 0) {
+            *member = sched_claim(a.sched) ? 1 : 0;
+            k = *member ? (int)blockIdx.x : total;
+        } else {
+            k = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        }
         ring.idx[sl] = k;
         mbar_arrive(&bars[kBarUnitFull + sl]);
         if (k >= total) break;
@@ -734,6 +776,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    volatile int* member = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 12);   // holds the counter slot
     const UnitRing ring{bars + kBarUnitFull, bars + kBarUnitEmpty,
                         reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -758,6 +801,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             mbar_init(&bars[kBarKV + C::kStages + s], 2);        // kv_empty: one commit per MMA stream
         }
         *abort_flag = 0;
+        *member = 0;
         fence_mbar_init();
     }
     if (warp == kWarpProducer && lane == 0) {
@@ -788,7 +832,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kWarpProducer) {
-            if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, a);
+            if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, sQ, sKV, bars, ring, abort_flag, member, a);
             __syncwarp();
         } else if (warp == kWarpMma0 || warp == kWarpMma1) {
             const int t = warp - kWarpMma0;
@@ -806,13 +850,7 @@ attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     // The last CTA out returns the launch's counters to zero for the next launch
     // that draws this slot.
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-            atomicExch(a.sched, 0u);
-            atomicExch(a.sched + 1, 0u);
-        }
-    }
+    if (threadIdx.x == 0 && *member) sched_release(a.sched);
 }
 }  // namespace
 }  // namespace bos
@@ -866,6 +904,7 @@ constexpr double kGroupKvBytes = 32.0 * 1024 * 1024;
 
 uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
 int g_test_stall = 0;
+int g_test_sched_busy = 0;
 std::atomic<unsigned int> g_sched_next{0};
 
 template <int D, bool kF16>
@@ -939,7 +978,16 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     a.lse = p.lse;
     a.wait_limit_ns = g_wait_limit_ns;
     a.test_stall = g_test_stall;
-    a.sched = sched + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    a.sched = sched + kSchedWords * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    // test hook: the drawn slot is marked as held by another launch for the
+    // duration of this one, so every CTA finds it busy
+    static const unsigned long long kForeignTag = ~0ull;
+    if (g_test_sched_busy &&
+        cudaMemcpyAsync(a.sched + 2, &kForeignTag, sizeof(kForeignTag), cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
     const int64_t units = (int64_t)BH * a.U;
     const int grid = (int)(units < sms ? units : sms);
     cudaLaunchConfig_t cfg = {};
@@ -955,6 +1003,10 @@ int launch_d(const AttnParams& p, cudaStream_t stream, int dev) {
     if (cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, a) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_LAUNCH;
+    }
+    if (g_test_sched_busy && cudaMemsetAsync(a.sched + 2, 0, sizeof(unsigned long long), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
     }
     return ATTN_OK;
 }
@@ -977,6 +1029,8 @@ int launch_attn_fwd(const AttnParams& p, cudaStream_t stream, int dev) {
 void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs; }
 
 void set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
+
+void set_test_sched_busy(int on) { g_test_sched_busy = on ? 1 : 0; }
 
 int read_and_clear_device_status(cudaStream_t stream) {
     int h = 0;

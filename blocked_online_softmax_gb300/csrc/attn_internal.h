@@ -53,6 +53,11 @@ void set_wait_limit_ns(uint64_t ns);
 // that nothing signals, so the bounded wait expires and the abort path runs.
 void set_test_stall(int on);
 
+// Test hook: launches enqueued while on find their work-counter slot held by
+// another launch (a foreign tag is written into it before the launch and
+// cleared after), so they take no units and record ATTN_ERR_SCHED_BUSY.
+void set_test_sched_busy(int on);
+
 // Synchronises `stream`, returns the sticky device status (an attn_status) and
 // clears it.
 int read_and_clear_device_status(cudaStream_t stream);

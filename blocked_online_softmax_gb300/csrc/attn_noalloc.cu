@@ -7,10 +7,15 @@
 //
 // Instead of stream-ordered staging memory, Q, K, V, O and LSE are staged
 // through one file-scope device array of ATTN_NOALLOC_SCRATCH_BYTES. The array
-// belongs to this translation unit's module, so a device holds it from the
-// first call on that device until the process exits.
+// belongs to this translation unit's module: a device holds it from the moment
+// that module is loaded on it until the process exits. With CUDA's default
+// lazy module loading that is the first call of this entry point on the
+// device (the address look-up below loads it); with CUDA_MODULE_LOADING=EAGER
+// it is the creation of the device's context, whether or not this entry point
+// is ever called.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -53,15 +58,18 @@ extern "C" int attn_fwd_host_noalloc(const void* q_h, const void* k_h, const voi
                                      float* lse_h, int B, int H, int N, int d, float scale, int causal,
                                      void* stream_) {
     if (!q_h || !k_h || !v_h || !o_h || !lse_h) return ATTN_ERR_NULLPTR;
+    // The same argument rules as attn_fwd_host, in the same order, before any
+    // size arithmetic (so no product below can overflow).
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_BAD_SHAPE;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_D;
+    if ((int64_t)B * H > INT_MAX || (int64_t)B * H * N > ((int64_t)1 << 40)) return ATTN_ERR_BAD_SHAPE;
+    if (d < 8 || d > 256 || d % 8 != 0) return ATTN_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return ATTN_ERR_BAD_SCALE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_ARG;
+    // rows <= 2^40 and d <= 256: every byte count below stays under 2^50
     const uint64_t rows = (uint64_t)B * (uint64_t)H * (uint64_t)N;
     const uint64_t tbytes = rows * (uint64_t)d * 2u;         // one bf16 tensor
     const uint64_t lbytes = rows * 4u;                       // fp32 LSE
-    if (tbytes > kScratchBytes || 4 * round256(tbytes) + round256(lbytes) > kScratchBytes)
-        return ATTN_ERR_TOO_LARGE;
+    if (4 * round256(tbytes) + round256(lbytes) > kScratchBytes) return ATTN_ERR_TOO_LARGE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {

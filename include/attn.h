@@ -42,7 +42,9 @@ typedef enum attn_status {
     ATTN_ERR_TIMEOUT = 8,            /* a bounded wait inside the kernel gave up */
     ATTN_ERR_CUDA = 9,               /* another CUDA runtime call failed */
     ATTN_ERR_BAD_ARG = 10,           /* causal not 0/1, or another malformed argument */
-    ATTN_ERR_TOO_LARGE = 11          /* the problem does not fit attn_fwd_host_noalloc's fixed scratch */
+    ATTN_ERR_TOO_LARGE = 11,         /* the problem does not fit attn_fwd_host_noalloc's fixed scratch */
+    ATTN_ERR_SCHED_BUSY = 12         /* (device status) a forward launch found its work-counter slot held by
+                                        another launch still in flight and skipped its work */
 } attn_status;
 
 /*
@@ -74,9 +76,17 @@ typedef enum attn_status {
  * writes nothing. On success the kernel is enqueued on `stream` and the call
  * returns without synchronising. Safe to call from several host threads.
  * May be captured in a CUDA graph (it allocates nothing and only enqueues
- * work on `stream`). Each launch draws a slot of work counters, and a
- * captured launch keeps its slot, so one graph instance must not be replayed
- * on two streams at the same time.
+ * work on `stream`).
+ *
+ * Work distribution: each launch draws one of 4096 slots of work counters in a
+ * static device array, round-robin, and its CTAs take work units from it. A
+ * slot is held by the launch (tagged with the launch's unique grid id) from
+ * its first CTA's start until its last CTA's end. A launch that finds its slot
+ * still held by another launch in flight (more than 4096 forward launches
+ * outstanding at once, or one graph instance, which keeps the slot it drew
+ * at capture, replayed on two streams at the same time) does not share that
+ * launch's counter: it skips its work, leaves its outputs incomplete and
+ * records ATTN_ERR_SCHED_BUSY, which attn_device_status reports.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int N, int d, float scale, int causal, void* stream);
@@ -151,20 +161,27 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
  *
  * The pages have no counterpart to this call. attn_fwd_host stages the host
  * arrays through device memory it allocates (from a memory pool) on every
- * call; some callers cannot allocate at that point (another framework's caching allocator owns the
- * device memory, or the thread must not take the implicit synchronisation an
- * allocation can bring). This entry point computes the same result with no
- * cudaMalloc, cudaMallocAsync or cudaFree: Q, K, V, O and LSE are staged
- * through one fixed device array of ATTN_NOALLOC_SCRATCH_BYTES, held by every
- * device the call has run on until the process exits.
+ * call; some callers cannot allocate at that point (another framework's
+ * caching allocator owns the device memory, or the thread must not take the
+ * implicit synchronisation an allocation can bring). This entry point
+ * computes the same result, byte for byte, with no cudaMalloc,
+ * cudaMallocAsync or cudaFree: Q, K, V, O and LSE are staged through one
+ * fixed device array of ATTN_NOALLOC_SCRATCH_BYTES.
  *
- *   arguments as for attn_fwd_host (host arrays, owned by the caller).
+ *   arguments as for attn_fwd_host (host arrays owned by the caller; d a
+ *   multiple of 8 from 8 to 256; the same status codes, checked in the same
+ *   order).
  *
  * Limit: 4 * round_up(B*H*N*d*2, 256) + round_up(B*H*N*4, 256) bytes must fit
  * in ATTN_NOALLOC_SCRATCH_BYTES (e.g. B*H*N*d up to about 8M elements);
  * larger problems return ATTN_ERR_TOO_LARGE before anything is copied.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.
+ * The array belongs to the library's module: a device holds it from when that
+ * module is loaded on it until the process exits. Under CUDA's default lazy
+ * loading that is this call's first use on the device; under
+ * CUDA_MODULE_LOADING=EAGER it is the creation of the device's context.
+ * The first call on a device also looks up the array's device address (with
+ * that device current) and keeps it; make that first call before any stream
+ * capture begins.
  * Every call shares the one array: calls whose work overlaps on the GPU (on
  * different streams, or from different host threads) race and must be
  * serialised by the caller. Nothing in the array needs clearing between calls:
@@ -202,6 +219,15 @@ int attn_set_wait_limit_ns(unsigned long long ns);
  * hang is involved. Process-wide; off by default.
  */
 int attn_set_test_stall(int on);
+
+/*
+ * attn_set_test_sched_busy - test hook for the work-counter guard. While `on`
+ * is nonzero, each forward launch's counter slot is marked as held by another
+ * launch (a copy on `stream` before the launch; the mark is cleared by a copy
+ * after it), so the launch skips its work and attn_device_status reports
+ * ATTN_ERR_SCHED_BUSY. Process-wide; off by default.
+ */
+int attn_set_test_sched_busy(int on);
 
 /* Human-readable text for a status code; never NULL, static storage. */
 const char* attn_status_string(int status);

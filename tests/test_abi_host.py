@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, 12):
+    for code in range(0, 13):
         s = bos.attn_status_string(code)
         assert s and s != "unknown status"
     assert bos.attn_status_string(12345) == "unknown status"

@@ -90,3 +90,28 @@ def test_backward_wait_timeout_is_reported_and_context_survives(d, causal):
     for name, gpu, ref in zip(("dq", "dk", "dv"), grads, oracle.attention_bwd(qh, kh, vh, gh, scale, causal)):
         err = np.abs(gpu.float().cpu().numpy() - ref).max()
         assert err <= 2e-2 * np.abs(ref).max() + 1e-3, f"{name}: {err}"
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True), (256, False)])
+def test_busy_counter_slot_is_reported_not_shared(d, causal):
+    """A launch whose work-counter slot is still held by another launch takes no
+    work units and records ATTN_ERR_SCHED_BUSY (it never shares the other
+    launch's counter). The hook marks the slot as held; no wait is involved.
+    The outputs stay untouched, and the next launch on a free slot is correct."""
+    qh, kh, vh = make_qkv(2, 8, 1024, d, seed=25)
+    q, k, v = (t.cuda() for t in (qh, kh, vh))
+    assert bos.attn_device_status() == bos.ATTN_OK
+    o = torch.full_like(q, -12288.0)
+    lse = torch.full((2, 8, 1024), -7.0e30, dtype=torch.float32, device=q.device)
+    bos.attn_set_test_sched_busy(True)
+    try:
+        bos.attn_fwd(q, k, v, o, lse, 2, 8, 1024, d, 0.1, causal)
+        status = bos.attn_device_status()
+    finally:
+        bos.attn_set_test_sched_busy(False)
+    assert status == bos.ATTN_ERR_SCHED_BUSY
+    assert torch.all(o == -12288.0) and torch.all(lse == -7.0e30), "a launch without its slot wrote output"
+    o, lse = _run(q, k, v, 0.1, causal)
+    assert bos.attn_device_status() == bos.ATTN_OK
+    o_ref, lse_ref = oracle.attention(qh, kh, vh, float(np.float32(0.1)), causal)
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "after a busy slot")
