@@ -310,7 +310,8 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
         const int tile_row0 = u.row0;
         const int row = tile_row0 + row_in_tile;
         float m_ref = -INFINITY;   // max the exponentials are taken against (base-2 units)
-        float l = 0.f;
+        float l = 0.f;     // sum of the fp32 probabilities (LSE)
+        float l_o = 0.f;   // the same plus each block's top-term rounding error (normalises O)
         for (int i = 0; i < u.n; ++i) {
             const int j = u.n - 1 - i;
             const uint32_t g = blocks;
@@ -325,7 +326,8 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
                 const int last = a.causal ? min(a.N, row + 1) : a.N;
                 mask_row(sr, c, need_mask ? max(0, min(kBN, last - key0)) : kBN);
             }
-            const float m_tile = (cs >= 0.f) ? row_extreme<true>(sr) * cs : row_extreme<false>(sr) * cs;
+            const float r_ext = (cs >= 0.f) ? row_extreme<true>(sr) : row_extreme<false>(sr);
+            const float m_tile = r_ext * cs;
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 m_ref = m_tile;
@@ -335,6 +337,7 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
             }
             const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint64_t negm2 = f2_pack(negm, negm);
+            const float top_err = top_rounding_error<kF16>(r_ext, cs, negm);
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {   // all 128 keys as bf16 pairs over the buffer's first 64 columns
@@ -362,13 +365,14 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
             float sum0, sum1;
             f2_unpack(s01, sum0, sum1);
             l = l * alpha + (sum0 + sum1);
+            l_o = l_o * alpha + (sum0 + sum1) + top_err;
         }
         if (!ok) break;
         // epilogue: the unit's last PV must be complete
         if (!wait_warp(&bars[kBarPvDone], (blocks - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const float l_safe = (l > 0.f) ? l : 1.f;
-        const float inv = 1.f / l_safe;
+        const float inv = 1.f / ((l_o > 0.f) ? l_o : 1.f);
 #pragma unroll 1
         for (int s = 0; s < nb; ++s) {
             uint32_t o0[32], o1[32];   // this slice's 64 columns of O

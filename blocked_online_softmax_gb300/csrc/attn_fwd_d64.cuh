@@ -265,7 +265,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         const int row = tile_row0 + row_in_tile;
         const int first = (t == 0) ? u.first0 : 0;
         float m_ref = -INFINITY;   // max the exponentials are taken against (base-2 units)
-        float l = 0.f;
+        float l = 0.f;     // sum of the fp32 probabilities (LSE)
+        float l_o = 0.f;   // the same plus each block's top-term rounding error (normalises O)
         for (int i = first; i < u.n; ++i) {
             const int j = u.n - 1 - i;
             if (!wait_warp(s_full, s_phase)) { ok = false; break; }
@@ -281,7 +282,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 const int last = a.causal ? min(a.N, row + 1) : a.N;
                 mask_row(sr, c, need_mask ? max(0, min(kBN, last - key0)) : kBN);
             }
-            const float m_tile = (cs >= 0.f) ? row_extreme<true>(sr) * cs : row_extreme<false>(sr) * cs;
+            const float r_ext = (cs >= 0.f) ? row_extreme<true>(sr) : row_extreme<false>(sr);
+            const float m_tile = r_ext * cs;
             // PV of the previous block (phase blocks-1) must be complete before a
             // half of P_t is rewritten (pa: keys 0-63, pb: keys 64-127 and O_t).
             const bool prev = blocks > 0;
@@ -295,6 +297,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             }
             const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint64_t negm2 = f2_pack(negm, negm);
+            const float top_err = top_rounding_error<kF16>(r_ext, cs, negm);
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             if (prev && !wait_warp(pa_done, par)) { ok = false; break; }
             tc_fence_after();
@@ -329,13 +332,14 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             float sum0, sum1;
             f2_unpack(s01, sum0, sum1);
             l = l * alpha + (sum0 + sum1);
+            l_o = l_o * alpha + (sum0 + sum1) + top_err;
         }
         if (!ok) break;
         // epilogue: O / l -> bf16 through the staging buffer and TMA, LSE in natural log
         if (!wait_warp(pb_done, (blocks - 1) & 1)) { ok = false; break; }   // the unit's last PV is complete
         tc_fence_after();
         const float l_safe = (l > 0.f) ? l : 1.f;
-        const float inv = 1.f / l_safe;
+        const float inv = 1.f / ((l_o > 0.f) ? l_o : 1.f);
         uint32_t ov[kD];
         uint32_t (&h0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[0]);
         uint32_t (&h1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[32]);

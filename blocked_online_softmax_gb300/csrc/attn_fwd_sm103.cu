@@ -544,6 +544,25 @@ __device__ __forceinline__ void mask_row(uint32_t (&sr)[128], float c, int lim) 
     for (int e = 0; e < 128; ++e) sr[e] = (e < lim) ? (sr[e] & keep) : masked;
 }
 
+// Rounding error of a block's largest probability in the element type P is
+// multiplied in. The PV product uses the rounded P, so adding this error to the
+// normaliser of O keeps the dominant term's weight exact in O = PV / l: a near
+// one-hot row (large logits) then reproduces its V row to within O's own
+// rounding, where the plain fp32 sum would leave the top term off by up to half
+// a bf16 unit in the last place. r_ext is the block's raw extreme score; the
+// exponent is formed exactly as exp_pack forms every element's.
+template <bool kF16>
+__device__ __forceinline__ float top_rounding_error(float r_ext, float cs, float negm) {
+    const float p = ex2(fmaf(r_ext, cs, negm));
+    float pr;
+    if constexpr (kF16) {
+        pr = __half2float(__float2half_rn(p));
+    } else {
+        pr = __bfloat162float(__float2bfloat16_rn(p));
+    }
+    return pr - p;
+}
+
 // exp2 of 32 scores (keys 32*ch .. 32*ch+31): x = s * c - m in one packed FMA per
 // pair, p = 2^x (masked columns hold the raw value whose x is -inf, see
 // mask_row), packed into 16 bf16 pairs (key 2e in the low half of pk[e]); the
@@ -641,7 +660,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         const int row = tile_row0 + row_in_tile;
         const int first = (t == 0) ? u.first0 : 0;
         float m_ref = -INFINITY;   // max the exponentials are taken against (base-2 units)
-        float l = 0.f;
+        float l = 0.f;     // sum of the fp32 probabilities (LSE)
+        float l_o = 0.f;   // the same plus each block's top-term rounding error (normalises O)
         for (int i = first; i < u.n; ++i) {
             const int j = u.n - 1 - i;
             if (!wait_warp(s_full, s_phase)) { ok = false; break; }
@@ -656,7 +676,8 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 const int last = a.causal ? min(a.N, row + 1) : a.N;
                 mask_row(sr, c, need_mask ? max(0, min(kBN, last - key0)) : kBN);
             }
-            const float m_tile = (cs >= 0.f) ? row_extreme<true>(sr) * cs : row_extreme<false>(sr) * cs;
+            const float r_ext = (cs >= 0.f) ? row_extreme<true>(sr) : row_extreme<false>(sr);
+            const float m_tile = r_ext * cs;
             // PV_hi of the previous block must be complete before O_t is rescaled
             // or the shared half of P_t is rewritten.
             bool pb_pending = (i > first);
@@ -671,6 +692,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             }
             const float negm = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint64_t negm2 = f2_pack(negm, negm);
+            const float top_err = top_rounding_error<kF16>(r_ext, cs, negm);
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f pairs
             // keys 0-63 into tensor memory; the MMA takes them (and then computes the
             // next block's scores) while keys 64-127 are being exponentiated
@@ -712,6 +734,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             float sum0, sum1;
             f2_unpack(s01, sum0, sum1);
             l = l * alpha + (sum0 + sum1);
+            l_o = l_o * alpha + (sum0 + sum1) + top_err;
         }
         if (!ok) break;
         // epilogue: O / l -> bf16 through shared memory and TMA, LSE in natural log
@@ -719,7 +742,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
         pb_phase ^= 1;
         tc_fence_after();
         const float l_safe = (l > 0.f) ? l : 1.f;
-        const float inv = 1.f / l_safe;
+        const float inv = 1.f / ((l_o > 0.f) ? l_o : 1.f);
         // One slice at a time, loaded from tensor memory per slice: the loop
         // stays rolled, so this once-per-unit code is half as large in the
         // instruction cache (8K causal: +1.5 % over a fully unrolled copy).

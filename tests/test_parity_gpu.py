@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
-Small and medium sizes are compared element by element over every output;
-the full-size workloads are compared on sampled rows (tile edges, the ragged
-tail, random rows) plus properties that hold at any size.
+Every measured workload is compared element by element over every output, at
+full size; only the very long single-head sequences (up to 65536 rows) are
+compared on sampled rows (tile edges, the ragged tail, random rows) plus
+properties that hold at any size.
 """
 import numpy as np
 import pytest
@@ -190,15 +191,18 @@ def test_host_buffer_entry_chunked_matches_device_entry():
                   "host entry, chunked")
 
 
-# ------------------------------------------------------------------ full-size workloads, sampled
+# ------------------------------------------------------------------ full-size workloads, every row
 
-@pytest.mark.parametrize("w", [MEDIUM, CAUSAL_2K, CAUSAL_8K, TAIL_4000, CAUSAL_4K_D256, WIDE_2K_D256],
+@pytest.mark.parametrize("w", [CAUSAL_2K, CAUSAL_8K, TAIL_4000, CAUSAL_4K_D256, WIDE_2K_D256],
                          ids=lambda w: w.name)
-def test_workload_full_size_sampled(w):
+def test_workload_full_size_every_row(w):
+    """The measured workloads at full size, in the bench's launch configuration,
+    compared with the oracle at every (batch, head, row) (the two smaller ones
+    are in test_workload_full). The oracle needs about 1 s (2K causal) to 15 s
+    (the 4000-row tail workload) on 16 host cores."""
     q, k, v = workload_qkv(w)
     o, lse = run_guarded(q, k, v, w.scale, w.causal)
-    # properties at every row: finite, and O a convex combination of V rows per column
-    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    # a property at every row as well: O is a convex combination of the V rows it sees
     vf = v.float()
     if not w.causal:
         vmax = vf.amax(dim=2, keepdim=True).numpy()
@@ -208,10 +212,8 @@ def test_workload_full_size_sampled(w):
         vmin = torch.cummin(vf, dim=2).values.numpy()
     slack = 1e-2 + 2 ** -7 * np.maximum(np.abs(vmax), np.abs(vmin))
     assert np.all(o <= vmax + slack) and np.all(o >= vmin - slack), "O outside the hull of V"
-    rows = sample_rows(w.B, w.H, w.N, seed=w.seed)
-    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
-    d = w.d
-    assert_parity(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.name)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
+    assert_parity(o, lse, o_ref, lse_ref, w.name)
 
 
 # ------------------------------------------------------------------ strided layouts
