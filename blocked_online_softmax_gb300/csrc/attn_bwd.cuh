@@ -372,8 +372,8 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
             uint8_t* box = ds_row + (ch >> 1) * 16384;       // queries 32ch..32ch+31: chunks 4(ch&1)..+3
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(box + ((((ch & 1) * 4 + c) ^ ds_swz) << 4)) =
-                    make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+                st_shared16(smem_u32(box + ((((ch & 1) * 4 + c) ^ ds_swz) << 4)),
+                            make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]));
             if (ch == 1) {                                    // Y's first four dK steps need only these
                 tmem_st_wait();
                 tc_fence_before();
@@ -416,7 +416,7 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
                 wv.y = pack2<kF16>(__uint_as_float(vv[2]), __uint_as_float(vv[3]));
                 wv.z = pack2<kF16>(__uint_as_float(vv[4]), __uint_as_float(vv[5]));
                 wv.w = pack2<kF16>(__uint_as_float(vv[6]), __uint_as_float(vv[7]));
-                *reinterpret_cast<uint4*>(srow + hb * 16384 + ((c ^ (lane & 7)) << 4)) = wv;
+                st_shared16(smem_u32(srow + hb * 16384 + ((c ^ (lane & 7)) << 4)), wv);
             }
         }
         fence_proxy_async_smem();
@@ -489,8 +489,8 @@ __device__ void dq_role(const CUtensorMap* tm_dq, uint32_t tY, int w, int lane, 
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const int e = h * 64 + b * 32 + c * 4;
-                    *reinterpret_cast<uint4*>(slot + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                        make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    st_shared16(smem_u32(slot + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                                make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]));
                 }
             fence_proxy_async_smem();
             __syncwarp();

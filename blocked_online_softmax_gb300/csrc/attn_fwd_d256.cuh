@@ -379,7 +379,7 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
             tmem_ld32(tO + s * 64, o0);
             tmem_ld32(tO + s * 64 + 32, o1);
             uint8_t* ebuf = ewarp + (slices++ & 1) * Cfg::kEpiBytes;
-            uint8_t* erow = ebuf + lane * 128;
+            const uint32_t erow = smem_u32(ebuf + lane * 128);
             if (lane == 0) bulk_wait_read1();   // the store before last (same buffer) is done reading
             __syncwarp();
 #pragma unroll
@@ -390,7 +390,7 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
                 w.y = pack2<kF16>(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv);
                 w.z = pack2<kF16>(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv);
                 w.w = pack2<kF16>(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv);
-                *reinterpret_cast<uint4*>(erow + ((q ^ swz) << 4)) = w;
+                st_shared16(erow + ((q ^ swz) << 4), w);
             }
             fence_proxy_async_smem();
             __syncwarp();

@@ -238,7 +238,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
     const uint32_t tO = lane_base + kTmemO;
     const int row_in_tile = wq * 32 + lane;
     uint8_t* sEpit = sEpi + t * Cfg::kTileBytes;
-    uint8_t* erow = sEpit + row_in_tile * 128;
+    const uint32_t erow = smem_u32(sEpit + row_in_tile * 128);   // this row of the staging buffer
     uint8_t* ewarp = sEpit + wq * 32 * 128;   // this warp's 32 rows (4 KB, 1024-byte aligned)
     const int swz = row_in_tile & 7;
     const float c = a.scale_log2;
@@ -356,7 +356,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             w.y = pack2<kF16>(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
             w.z = pack2<kF16>(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
             w.w = pack2<kF16>(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
-            *reinterpret_cast<uint4*>(erow + ((q ^ swz) << 4)) = w;
+            st_shared16(erow + ((q ^ swz) << 4), w);
         }
         fence_proxy_async_smem();
         __syncwarp();

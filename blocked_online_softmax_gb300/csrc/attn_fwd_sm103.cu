@@ -598,7 +598,7 @@ __device__ __forceinline__ void p_lo_to_tmem(const uint32_t (&sr)[128], uint64_t
 // K-major with the 128-byte swizzle (16-byte chunk q of the row at q ^ (row & 7)).
 template <bool kF16>
 __device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t c2, uint64_t negm2,
-                                             uint64_t (&acc)[4], uint8_t* prow, int swz) {
+                                             uint64_t (&acc)[4], uint32_t prow, int swz) {
 #pragma unroll
     for (int ch = 2; ch < 4; ++ch) {
         uint32_t pk[16];
@@ -606,8 +606,7 @@ __device__ __forceinline__ void p_hi_to_smem(const uint32_t (&sr)[128], uint64_t
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int c16 = (ch - 2) * 4 + q;
-            *reinterpret_cast<uint4*>(prow + ((c16 ^ swz) << 4)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            st_shared16(prow + ((c16 ^ swz) << 4), make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
         }
     }
 }
@@ -632,7 +631,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
     const uint32_t tO = lane_base + kTmemO;
     const int row_in_tile = wq * 32 + lane;
     uint8_t* sPbt = sPb + t * C::kPbBytes;
-    uint8_t* prow = sPbt + row_in_tile * 128;
+    const uint32_t prow = smem_u32(sPbt + row_in_tile * 128);   // this row of the shared half of P
     uint8_t* pwarp = sPbt + wq * 32 * 128;   // this warp's 32 rows (4 KB, 1024-byte aligned)
     const int swz = row_in_tile & 7;
     const float c = a.scale_log2;
@@ -763,7 +762,7 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
                 w.y = pack2<kF16>(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv);
                 w.z = pack2<kF16>(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv);
                 w.w = pack2<kF16>(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv);
-                *reinterpret_cast<uint4*>(prow + ((q ^ swz) << 4)) = w;
+                st_shared16(prow + ((q ^ swz) << 4), w);
             }
             fence_proxy_async_smem();
             __syncwarp();

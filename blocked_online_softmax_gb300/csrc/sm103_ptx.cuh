@@ -79,6 +79,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+// 16 bytes to shared memory by a shared-window address. A store through a
+// generic pointer into dynamic shared memory compiles to a generic store; this
+// one is a native shared store.
+__device__ __forceinline__ void st_shared16(uint32_t saddr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
