@@ -258,7 +258,12 @@ int attn_abi_version(void);
  *                      the fp32 dq accumulator (every key block adds its part
  *                      with bulk tensor reductions) and the fp32 row sums D.
  *                      Owned by the caller; nothing is allocated.
- *   B, H, N, d, scale, causal, stream: as attn_fwd, with d up to 128.
+ *   B, H, N, d, scale, causal, stream: as attn_fwd, with d up to 128. Head
+ *                      dims above 128 are not supported, by design: one CTA
+ *                      per key block accumulates dK and dV (fp32, d columns
+ *                      each) in tensor memory, and at d = 256 those two alone
+ *                      take all 512 columns an SM has, before the columns of
+ *                      S^T, dP^T and dQ; ATTN_ERR_UNSUPPORTED_D is returned.
  *
  * Asynchronous on stream. Returns the attn_fwd validation codes, or
  * ATTN_ERR_BAD_ARG when the workspace is smaller than needed; on an error
