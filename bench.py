@@ -15,7 +15,9 @@ slowest rank's time ("weak" scaling).
 On one GPU the line also carries two records outside the timed region:
 ``per_config`` (forward and backward TFLOP/s on each of the five measured
 workloads, each timed by the same rule: L2 flushed before every launch when
-the inputs fit in it, back to back otherwise) and ``sustained`` (the default
+the inputs fit in it, back to back otherwise; workloads that fit in L2 are
+also timed back to back over rotating cold copies of their inputs, which
+leaves out the per-launch event pair's fixed cost) and ``sustained`` (the default
 workload back to back for about 1.5 s with the SM clock sampled, reported
 against the measured sustained peak as well).
 
@@ -376,6 +378,38 @@ def time_backward_steps(w, dev, steps):
     return t0.elapsed_time(t1) / steps, "back-to-back steps between two CUDA events (inputs larger than L2)"
 
 
+def time_forward_rotating(w, dev, launches):
+    """Mean device time of one forward launch on workload w, back to back over
+    rotating copies of the inputs whose total exceeds the 129 MB L2 (so each
+    launch still reads cold inputs), with no event or flush between launches:
+    the launch's own time without the fixed cost of the per-launch event pair."""
+    import torch
+
+    import blocked_online_softmax_gb300 as bos
+    from blocked_online_softmax_gb300.workloads import workload_qkv
+    base = workload_qkv(w)
+    in_bytes = 3 * base[0].numel() * 2
+    ncopy = max(2, int(math.ceil(260e6 / in_bytes)) + 1)
+    copies = []
+    for _ in range(ncopy):
+        q, k, v = (t.to(dev) for t in base)
+        copies.append((q, k, v, torch.empty_like(q), torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.Stream(device=dev)
+    run = lambda i: bos.attn_fwd(*copies[i % ncopy], w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+    with torch.cuda.stream(stream):
+        for i in range(2 * ncopy):
+            run(i)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(launches):
+            run(i)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    return t0.elapsed_time(t1) / launches, ncopy
+
+
 def per_config_record(dev, peak, peak_sus, launches=30, bwd_steps=10):
     """Forward and backward on every measured workload (the five of the survey's
     measurement table), each by the bench's timing rule."""
@@ -387,6 +421,15 @@ def per_config_record(dev, peak, peak_sus, launches=30, bwd_steps=10):
         rec = {"name": w.name, "workload": w.describe(), "fwd_tflops": tf, "fwd_frac": tf / peak,
                "fwd_frac_of_sustained": tf / peak_sus, "fwd_mean_launch_ms": ms, "fwd_launches": launches,
                "fwd_timing": mode}
+        if 3 * w.B * w.H * w.N * w.d * 2 <= 129e6:
+            # inputs that fit in L2: also back to back over rotating cold copies,
+            # which leaves out the per-launch event pair's fixed cost
+            rms, ncopy = time_forward_rotating(w, dev, 2 * launches)
+            rtf = w.flops / (rms / 1e3) / 1e12
+            rec.update({"fwd_rotating_tflops": rtf, "fwd_rotating_frac": rtf / peak,
+                        "fwd_rotating_mean_launch_ms": rms,
+                        "fwd_rotating_timing": f"back-to-back launches between two CUDA events over {ncopy} "
+                                               "rotating input copies (more than L2 in all)"})
         bms, bmode = time_backward_steps(w, dev, bwd_steps)
         btf = 2.5 * w.flops / (bms / 1e3) / 1e12
         rec.update({"bwd_tflops": btf, "bwd_frac": btf / peak, "bwd_mean_step_ms": bms,
