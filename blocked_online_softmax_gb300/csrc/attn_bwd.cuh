@@ -13,29 +13,30 @@
 // at the end. An optional gradient g on the LSE output enters as D_i - g_i
 // (the derivative of LSE_i in S_ij is P_ij).
 //
-// GB300 design: one CTA (352 threads) per (key block j of 128 keys, batch*head),
+// GB300 design: one CTA (512 threads) per (key block j of 128 keys, batch*head),
 // looping over the query blocks i of 128 queries that can see block j.
 // Measured on this GPU (microbenchmark): one thread issuing 128 x N x 16 bf16
 // MMAs into one tensor-memory allocation completes one every ~134 cycles for
 // any N up to 128, and only two threads issuing into two separate allocations
 // overlap. The five products of a block are therefore split over two issuing
 // warps, each with its own 256-column allocation:
-//   X (warp 9):  S^T = K Q_i^T into X[0,128); P^T comes back over its first
-//                64 columns as bf16 pairs; dV_j += P^T dO_i into X[128,128+d).
-//   Y (warp 10): dP^T = V dO_i^T into Y[0,128); dS^T comes back over its first
-//                64 columns; dK_j += dS^T Q_i into Y[128,128+d); then
+//   X (warp 13): S^T = K Q_i^T into X[0,128); P^T comes back over those
+//                columns as bf16 pairs; dV_j += P^T dO_i into X[128,128+d).
+//   Y (warp 14): dP^T = V dO_i^T into Y[0,128); dS^T comes back over those
+//                columns; dK_j += dS^T Q_i into Y[128,128+d); then
 //                dQ_i = dS K_j (fp32, query on the lane) into Y[0,128) for
 //                d = 128 (after dK has read dS^T, in issue order) or into
 //                Y[192,256) for d = 64.
 // Working with the transposes keeps the key on the tensor-memory lane, so the
 // dV and dK products take P^T and dS^T straight from tensor memory.
-// Warps 0-3 (thread = key = lane) form P = exp2(S c - L2) as soon as S^T lands
-// (X can then start dV and the next block's S^T), then dS = P (dP scale -
-// D scale) once dP^T lands; dS also goes to shared memory, each thread writing
-// its key's row of 128 queries with 16-byte stores ([key][query], 128-byte
+// Two compute warpgroups (thread = key = lane), warps 0-3 for queries 0-63 and
+// warps 8-11 for queries 64-127 of each block, form P = exp2(S c - L2) as soon
+// as S^T lands (X can then start dV and the next block's S^T), then dS = P (dP
+// scale - D scale) once dP^T lands. Both are elementwise in the query, so the
+// groups need no exchange; each packs its bf16 pairs over columns it has read
+// itself (see pcol). dS also goes to shared memory, each thread writing its
+// key's row of 64 queries with 16-byte stores ([key][query], 128-byte
 // swizzle): the A operand of the dQ product, read query-major (MN-major).
-// Scalar stores into a [query][key] layout cost eight times the store
-// instructions on the compute warps' path.
 // Warps 4-7 (thread = query = lane) take the dQ part out of tensor memory,
 // write it to shared memory (an 8 KB slot per warp, 128-byte swizzle) and add
 // it into the fp32 dQ buffer with TMA bulk tensor reductions, so the adds move
@@ -44,7 +45,7 @@
 // block's -LSE (base 2) and -D (times scale) in shared memory two blocks ahead,
 // their global loads issued a block before the store; negated, each pair of
 // queries costs the compute warps one packed f32x2 FMA per step.
-// Warp 8 issues the TMA loads: K_j and V_j once, Q_i into two stages and dO_i
+// Warp 12 issues the TMA loads: K_j and V_j once, Q_i into two stages and dO_i
 // into one (its next load has the dS and dK/dQ steps of a block to land).
 
 namespace bos {
@@ -52,11 +53,20 @@ namespace {
 
 namespace bwd {
 
-constexpr int kThreads = 352;
+// Warps 0-3 and 8-11: compute (queries 0-63 and 64-127 of every block); 4-7:
+// dQ; 12: TMA producer; 13, 14: MMA issuers; 15 idle. Registers after launch
+// (512 x 128), redistributed per warpgroup with setmaxnreg:
+// 128 x (kRegsCompute x 2 + kRegsDq + kRegsControl) = 65536.
+constexpr int kThreads = 512;
 constexpr int kWarpDq = 4;          // warps 4-7
-constexpr int kWarpProducer = 8;
-constexpr int kWarpMmaX = 9;        // also allocates both tensor-memory regions
-constexpr int kWarpMmaY = 10;
+constexpr int kWarpCompute1 = 8;    // warps 8-11: the second half of each block's queries
+constexpr int kWarpProducer = 12;
+constexpr int kWarpMmaX = 13;       // also allocates both tensor-memory regions
+constexpr int kWarpMmaY = 14;
+constexpr int kRegsCompute = 112;
+constexpr int kRegsDq = 184;
+constexpr int kRegsControl = 104;
+static_assert(2 * kRegsCompute + kRegsDq + kRegsControl == 512, "register split must use the launch's file");
 constexpr uint32_t kCols = 256;     // columns of each allocation
 constexpr uint32_t kAcc = 128;      // dV (in X) and dK (in Y) start at this column
 constexpr float kLog2e = 1.4426950408889634f;
@@ -69,15 +79,15 @@ enum : int {
     kBarDoFull = 5,    // dO_i has landed
     kBarDoEmpty = 6,   // the dO buffer is free: X's dV and Y's dP of its block are complete (2 commits)
     kBarSFull = 7,     // S^T of the block is complete (X commit)
-    kBarPReady = 8,    // P^T is written (128 arrivals)
+    kBarPReady = 8,    // P^T is written (256 arrivals: both compute warpgroups)
     kBarDpFull = 9,    // dP^T of the block is complete (Y commit)
-    kBarDsReady = 10,  // dS^T (tensor memory) and dS (shared memory) are written (128 arrivals)
+    kBarDsReady = 10,  // dS^T (tensor memory) and dS (shared memory) are written (256 arrivals)
     kBarDqReady = 11,  // the block's dQ part is complete (Y commit)
     kBarDqRead = 12,   // the dQ part has been read out of tensor memory (128 arrivals)
     kBarLseFull = 13,  // [2] LSE and D of a block are staged (128 arrivals)
     kBarDrainX = 15,   // every MMA of X is complete
     kBarDrainY = 16,   // every MMA of Y is complete
-    kBarDsHalf = 17,   // dS^T of queries 0-63 is written (128 arrivals): Y may start dK
+    kBarDsHalf = 17,   // dS^T of queries 0-63 is written (128 arrivals, the first compute warpgroup): Y may start dK
     kBarNever = 18,    // test hook: nothing arrives on it
     kNumBars = 19,
 };
@@ -102,6 +112,14 @@ struct Cfg {
     static constexpr uint32_t kTdQ = (D == 64) ? 192u : 0u;    // dQ columns in Y
     static_assert(kSmemBytes <= kMaxSmem, "shared memory over the per-CTA limit");
 };
+
+// Packed bf16 pairs of P^T / dS^T in tensor memory. Each compute warpgroup
+// writes over the S^T / dP^T columns of its own queries (group h reads columns
+// 64h..64h+63), so neither overwrites a column the other has yet to read:
+// 32-query chunk ch (queries 32ch..32ch+31) lands at columns pcol(ch)..+15,
+// and the 16-query MMA step kk reads its 8 columns at pcol_step(kk).
+__host__ __device__ constexpr uint32_t pcol(int ch) { return (uint32_t)(ch * 16 + (ch >= 2 ? 32 : 0)); }
+__host__ __device__ constexpr uint32_t pcol_step(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
 
 struct BwdArgs {
     int BH, H, N, d, nkv, causal;
@@ -215,7 +233,7 @@ __device__ void mma_x(uint32_t tX, uint8_t* smem, uint64_t* bars, volatile int* 
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // 16 queries per step: 8 columns of bf16 pairs, 16 rows of dO
-            mma_ts(tX + kAcc, tX + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), id_kv,
+            mma_ts(tX + kAcc, tX + pcol_step(kk), sdesc_sw128(sDO + kk * 2048, 16384, 1024), id_kv,
                    (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarDoEmpty]);
     }
@@ -260,13 +278,13 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tY + kAcc, tY + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv,
+            mma_ts(tY + kAcc, tY + pcol_step(kk), sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv,
                    (it > 0 || kk > 0) ? 1u : 0u);
         if (!wait_or_abort(&bars[kBarDsReady], (uint32_t)(it & 1), lim, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 4; kk < 8; ++kk)
-            mma_ts(tY + kAcc, tY + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv, 1u);
+            mma_ts(tY + kAcc, tY + pcol_step(kk), sdesc_sw128(sQ + kk * 2048, 16384, 1024), id_kv, 1u);
         mma_commit(&bars[kBarQEmpty + s]);
         if (!kDqOverDp && it > 0 && !wait_or_abort(&bars[kBarDqRead], (uint32_t)((it - 1) & 1), lim, abort_flag))
             break;
@@ -281,13 +299,15 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
     mbar_wait(&bars[kBarDrainY], 0, kDrainLimitNs);
 }
 
-// P^T of one block into tensor memory (over the S^T columns already read) and
-// into registers as bf16 pairs (queries 2e, 2e+1 of each 32-query chunk).
+// P^T of one block's queries 64h..64h+63 into tensor memory (over the S^T
+// columns already read) and into registers as bf16 pairs (queries 2e, 2e+1 of
+// each 32-query chunk).
 template <bool kMasked, bool kF16>
 __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c2x2, int r, bool key_ok, bool diag,
-                                        uint32_t (&pk)[64]) {
+                                        int h, uint32_t (&pk)[32]) {
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * h + cc;
         uint32_t sv[32];
         tmem_ld32(lx + ch * 32, sv);
         uint32_t t[16];
@@ -303,15 +323,19 @@ __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c
                 if (!key_ok || (diag && qc + 1 < r)) p1 = 0.f;
             }
             t[e] = pack2<kF16>(p0, p1);
-            pk[ch * 16 + e] = t[e];
+            pk[cc * 16 + e] = t[e];
         }
-        tmem_st16(lx + ch * 16, t);
+        tmem_st16(lx + pcol(ch), t);
     }
 }
 
+// Compute warpgroup h (0: queries 0-63 of each block, 1: queries 64-127); the
+// two groups share the keys (tensor-memory lanes) and need no exchange: P and
+// dS are elementwise in the query. After the loop group 0 writes dV_j and
+// group 1 writes dK_j.
 template <int D, bool kF16>
 __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv, uint32_t tX, uint32_t tY, int w,
-                             int lane, uint8_t* smem, uint64_t* bars,
+                             int h, int lane, uint8_t* smem, uint64_t* bars,
                              volatile int* abort_flag, int bh, int j, int nq, const BwdArgs& a) {
     using C = Cfg<D>;
     const uint64_t lim = a.wait_limit_ns;
@@ -340,11 +364,11 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
         const float* L = lse_s + lb * 128;
         const float* Dsc = dsc_s + lb * 128;
         const bool diag = a.causal && it == 0;               // the first query block is block j itself
-        uint32_t pk[64];
+        uint32_t pk[32];
         if (diag || tail_block)
-            p_phase<true, kF16>(lx, L, c2x2, r, key_ok, diag, pk);
+            p_phase<true, kF16>(lx, L, c2x2, r, key_ok, diag, h, pk);
         else
-            p_phase<false, kF16>(lx, L, c2x2, r, key_ok, diag, pk);
+            p_phase<false, kF16>(lx, L, c2x2, r, key_ok, diag, h, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kBarPReady]);
@@ -352,7 +376,8 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
         if (!wait_warp(&bars[kBarDpFull], par)) return;
         tc_fence_after();
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int cc = 0; cc < 2; ++cc) {
+            const int ch = 2 * h + cc;
             uint32_t dpv[32];
             tmem_ld32(ly + ch * 32, dpv);
             uint32_t dk[16];
@@ -360,7 +385,7 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
             for (int e = 0; e < 16; ++e) {
                 const int qc = ch * 32 + 2 * e;
                 const uint64_t nd = *reinterpret_cast<const uint64_t*>(Dsc + qc);
-                const uint32_t p = pk[ch * 16 + e];
+                const uint32_t p = pk[cc * 16 + e];
                 const uint64_t t2 =
                     f2_fma(f2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), scale2, nd);
                 float ds0, ds1, p0, p1;
@@ -368,7 +393,7 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
                 f2_unpack(f2_mul(f2_pack(p0, p1), t2), ds0, ds1);
                 dk[e] = pack2<kF16>(ds0, ds1);
             }
-            tmem_st16(ly + ch * 16, dk);                      // dS^T over dP^T columns already read
+            tmem_st16(ly + pcol(ch), dk);                     // dS^T over dP^T columns this group has read
             uint8_t* box = ds_row + (ch >> 1) * 16384;       // queries 32ch..32ch+31: chunks 4(ch&1)..+3
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -377,7 +402,7 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
             if (ch == 1) {                                    // Y's first four dK steps need only these
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars[kBarDsHalf]);
+                mbar_arrive(&bars[kBarDsHalf]);                // group 0 only
             }
         }
         tmem_st_wait();
@@ -394,7 +419,7 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
     const int b_idx = bh / a.H, h_idx = bh % a.H;
     bool drained = true;
 #pragma unroll 1
-    for (int pass = 0; pass < 2 && drained; ++pass) {
+    for (int pass = h; pass < h + 1 && drained; ++pass) {
         if (!wait_warp(&bars[pass == 0 ? kBarDrainX : kBarDrainY], 0)) {
             drained = false;
             break;
@@ -545,9 +570,9 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_init(&bars[bwd::kBarDoFull], 1);
         mbar_init(&bars[bwd::kBarDoEmpty], 2);
         mbar_init(&bars[bwd::kBarSFull], 1);
-        mbar_init(&bars[bwd::kBarPReady], 128);
+        mbar_init(&bars[bwd::kBarPReady], 256);
         mbar_init(&bars[bwd::kBarDpFull], 1);
-        mbar_init(&bars[bwd::kBarDsReady], 128);
+        mbar_init(&bars[bwd::kBarDsReady], 256);
         mbar_init(&bars[bwd::kBarDqReady], 1);
         mbar_init(&bars[bwd::kBarDqRead], 128);
         mbar_init(&bars[bwd::kBarDrainX], 1);
@@ -576,19 +601,25 @@ attn_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tc_fence_after();
     const uint32_t tX = tmem_slot[0], tY = tmem_slot[1];
 
-    if (warp < bwd::kWarpDq) {
-        bwd::compute_role<D, kF16>(&tm_dk, &tm_dv, tX, tY, warp, lane, smem, bars, abort_flag, bh, j, nq, a);
-    } else if (warp < bwd::kWarpProducer) {
+    if (warp < bwd::kWarpDq || (warp >= bwd::kWarpCompute1 && warp < bwd::kWarpProducer)) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(bwd::kRegsCompute));
+        bwd::compute_role<D, kF16>(&tm_dk, &tm_dv, tX, tY, warp & 3, warp < bwd::kWarpDq ? 0 : 1, lane, smem, bars,
+                                   abort_flag, bh, j, nq, a);
+    } else if (warp < bwd::kWarpCompute1) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(bwd::kRegsDq));
         bwd::dq_role<D>(&tm_dq, tY, warp, lane, smem, bars, abort_flag, bh, i0, nq, a);
-    } else if (warp == bwd::kWarpProducer) {
-        if (lane == 0) bwd::producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, smem, bars, abort_flag, bh, j, i0, nq, a);
-        __syncwarp();
-    } else if (warp == bwd::kWarpMmaX) {
-        if (lane == 0) bwd::mma_x<D, kF16>(tX, smem, bars, abort_flag, nq, a);
-        __syncwarp();
     } else {
-        if (lane == 0) bwd::mma_y<D, kF16>(tY, smem, bars, abort_flag, nq, a);
-        __syncwarp();
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(bwd::kRegsControl));
+        if (warp == bwd::kWarpProducer) {
+            if (lane == 0) bwd::producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, smem, bars, abort_flag, bh, j, i0, nq, a);
+            __syncwarp();
+        } else if (warp == bwd::kWarpMmaX) {
+            if (lane == 0) bwd::mma_x<D, kF16>(tX, smem, bars, abort_flag, nq, a);
+            __syncwarp();
+        } else if (warp == bwd::kWarpMmaY) {
+            if (lane == 0) bwd::mma_y<D, kF16>(tY, smem, bars, abort_flag, nq, a);
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
