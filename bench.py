@@ -29,6 +29,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -92,12 +93,22 @@ def job_throughput(flops_per_step: float, steps: int, world: int, seconds: float
     return flops_per_step * steps * world / seconds / 1e12
 
 
+def code_without_comments(text: str) -> str:
+    """C/C++/CUDA source with its comments and blank lines removed and each line
+    stripped (these sources hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).strip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the attention kernel's sources (the counters in profiles/ are tied to it)."""
+    """Hash of the attention kernel's code (the counters in profiles/ are tied to
+    it); comments do not enter it, so a comment-only edit keeps the counters."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(os.path.basename(rel).encode() + b"\0" + f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            code = code_without_comments(f.read())
+        h.update(os.path.basename(rel).encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

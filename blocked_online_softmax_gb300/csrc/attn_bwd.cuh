@@ -15,11 +15,10 @@
 //
 // GB300 design: one CTA (512 threads) per (key block j of 128 keys, batch*head),
 // looping over the query blocks i of 128 queries that can see block j.
-// Measured on this GPU (microbenchmark): one thread issuing 128 x N x 16 bf16
-// MMAs into one tensor-memory allocation completes one every ~134 cycles for
-// any N up to 128, and only two threads issuing into two separate allocations
-// overlap. The five products of a block are therefore split over two issuing
-// warps, each with its own 256-column allocation:
+// MMAs issued by one thread execute in issue order, so the five products of a
+// block are split over two issuing warps, each with its own 256-column
+// allocation, by what they wait on: X waits only for P, Y for dS and for the
+// dQ read-out, and neither chain holds back the other's MMAs.
 //   X (warp 13): S^T = K Q_i^T into X[0,128); P^T comes back over those
 //                columns as bf16 pairs; dV_j += P^T dO_i into X[128,128+d).
 //   Y (warp 14): dP^T = V dO_i^T into Y[0,128); dS^T comes back over those

@@ -20,8 +20,9 @@
 //    and Q tile 1, one thread per query row, with 208 registers each after a
 //    setmaxnreg split; warp 8 takes units and issues TMA loads (Q per unit, then
 //    K_j, V_j into a multi-stage ring); warps 9 and 10 each issue the tcgen05
-//    MMAs of one Q tile from one thread (two independent MMA streams keep the
-//    tensor core busy; one stream alone cannot).
+//    MMAs of one Q tile from one thread. A stream executes its MMAs in issue
+//    order, and each tile's products wait on its own softmax; with a stream
+//    per tile, one tile's waits do not hold back the other tile's MMAs.
 //  * Tensor memory: one 256-column allocation per Q tile holding S_t = Q_t K^T
 //    (fp32, 128 columns) and O_t (fp32, d columns). Keys 0-63 of P_t are written
 //    back as bf16 over S_t's first 32 columns and multiplied from there (TS
@@ -73,10 +74,10 @@ constexpr int kRegsSoftmax = 208;
 constexpr int kRegsControl = 88;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
 // Each Q tile has its own 256-column TMEM allocation: S at column 0 (P overlays
-// its first 64 columns as packed bf16), O at column 128. The tensor core keeps
-// MMAs of one issuing thread into one allocation in order, one at a time; two
-// allocations fed by two warps run concurrently, which is what lets 128-wide
-// MMAs reach the tensor core's full rate.
+// its first 64 columns as packed bf16), O at column 128. MMAs issued by one
+// thread run in issue order; one thread issuing 128 x 128 x 16 MMAs back to
+// back keeps the tensor core at 94-100 % of its rate (measured on this GPU),
+// and two threads issuing at once share it.
 constexpr uint32_t kTmemColsPerTile = 256;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;

@@ -21,6 +21,15 @@ def test_kernel_source_hash_is_stable():
     assert len(bench.kernel_source_hash()) == 16
 
 
+def test_source_hash_ignores_comments_only():
+    code = "int f(int x) {\n    return x + 1;   // one more\n}\n"
+    commented = "/* header\n   text */\nint f(int x) {\n\n    // a note\n    return x + 1;\n}\n"
+    changed = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench.code_without_comments(code) == bench.code_without_comments(commented)
+    assert bench.code_without_comments(code) != bench.code_without_comments(changed)
+    assert bench.code_without_comments('asm("max.f32 %0, %1;");  // 2-input') == 'asm("max.f32 %0, %1;");'
+
+
 def test_clock_summary_flags_throttling():
     # index, sm MHz, max MHz, power, active reasons, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
     idle = ["0", "345", "2070", "100.0", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
