@@ -300,22 +300,26 @@ __device__ void mma_y(uint32_t tY, uint8_t* smem, uint64_t* bars, volatile int* 
 
 // P^T of one block's queries 64h..64h+63 into tensor memory (over the S^T
 // columns already read) and into registers as bf16 pairs (queries 2e, 2e+1 of
-// each 32-query chunk).
+// each 32-query chunk). The second chunk's scores are requested from tensor
+// memory before the first chunk's P^T is stored, so that load's latency
+// overlaps the store (the columns differ: see pcol).
 template <bool kMasked, bool kF16>
 __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c2x2, int r, bool key_ok, bool diag,
                                         int h, uint32_t (&pk)[32]) {
+    uint32_t sv[2][32];
+    tmem_ld32_nowait(lx + (2 * h) * 32, sv[0]);
+    tmem_ld_wait32(sv[0]);
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         const int ch = 2 * h + cc;
-        uint32_t sv[32];
-        tmem_ld32(lx + ch * 32, sv);
         uint32_t t[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int qc = ch * 32 + 2 * e;
             const uint64_t nl = *reinterpret_cast<const uint64_t*>(nL + qc);
             float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[cc][2 * e]), __uint_as_float(sv[cc][2 * e + 1])), c2x2, nl),
+                      x0, x1);
             float p0 = ex2(x0), p1 = ex2(x1);
             if (kMasked) {
                 if (!key_ok || (diag && qc < r)) p0 = 0.f;
@@ -324,7 +328,9 @@ __device__ __forceinline__ void p_phase(uint32_t lx, const float* nL, uint64_t c
             t[e] = pack2<kF16>(p0, p1);
             pk[cc * 16 + e] = t[e];
         }
+        if (cc == 0) tmem_ld32_nowait(lx + (ch + 1) * 32, sv[1]);
         tmem_st16(lx + pcol(ch), t);
+        if (cc == 0) tmem_ld_wait32(sv[1]);
     }
 }
 
@@ -374,24 +380,28 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
 
         if (!wait_warp(&bars[kBarDpFull], par)) return;
         tc_fence_after();
+        // the second chunk's dP^T is requested before the first chunk's dS is
+        // stored, so that load's latency overlaps the stores (disjoint columns)
+        uint32_t dpv[2][32];
+        tmem_ld32_nowait(ly + (2 * h) * 32, dpv[0]);
+        tmem_ld_wait32(dpv[0]);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
             const int ch = 2 * h + cc;
-            uint32_t dpv[32];
-            tmem_ld32(ly + ch * 32, dpv);
             uint32_t dk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int qc = ch * 32 + 2 * e;
                 const uint64_t nd = *reinterpret_cast<const uint64_t*>(Dsc + qc);
                 const uint32_t p = pk[cc * 16 + e];
-                const uint64_t t2 =
-                    f2_fma(f2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), scale2, nd);
+                const uint64_t t2 = f2_fma(f2_pack(__uint_as_float(dpv[cc][2 * e]), __uint_as_float(dpv[cc][2 * e + 1])),
+                                           scale2, nd);
                 float ds0, ds1, p0, p1;
                 unpack2<kF16>(p, p0, p1);
                 f2_unpack(f2_mul(f2_pack(p0, p1), t2), ds0, ds1);
                 dk[e] = pack2<kF16>(ds0, ds1);
             }
+            if (cc == 0) tmem_ld32_nowait(ly + (ch + 1) * 32, dpv[1]);
             tmem_st16(ly + pcol(ch), dk);                     // dS^T over dP^T columns this group has read
             uint8_t* box = ds_row + (ch >> 1) * 16384;       // queries 32ch..32ch+31: chunks 4(ch&1)..+3
 #pragma unroll
@@ -403,6 +413,7 @@ __device__ void compute_role(const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
                 tc_fence_before();
                 mbar_arrive(&bars[kBarDsHalf]);                // group 0 only
             }
+            if (cc == 0) tmem_ld_wait32(dpv[1]);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
