@@ -331,7 +331,7 @@ __device__ void softmax_role(uint32_t tm, int wq, int lane, uint64_t* bars, cons
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 m_ref = m_tile;
-            } else if (m_tile > m_ref + kRescaleThreshold) {
+            } else if (m_tile > m_ref + rescale_threshold<kF16>()) {
                 alpha = ex2(m_ref - m_tile);
                 m_ref = m_tile;
             }

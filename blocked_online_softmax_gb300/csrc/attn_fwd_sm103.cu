@@ -34,9 +34,10 @@
 //    (the causal diagonal, the ragged tail past N) come first. Causal: blocks
 //    past a tile's diagonal are skipped, as in the page's loop bound.
 //  * The running max is only moved (and O, l rescaled) when a block's max
-//    exceeds it by more than 8 in log2 units; otherwise exponentials are taken
-//    against the older, smaller max (p <= 2^8). O/l and LSE are unchanged in
-//    exact arithmetic, and the O rescale through tensor memory becomes rare.
+//    exceeds it by more than 32 in log2 units (8 with fp16 P); otherwise
+//    exponentials are taken against the older, smaller max (p <= 2^32). O/l
+//    and LSE are unchanged in exact arithmetic, and the O rescale through
+//    tensor memory becomes rare even for large logits.
 //  * Epilogue: O / l as bf16 through the tile's shared P buffer, one TMA store
 //    per warp (32 rows), fp32 LSE with plain stores.
 //  * Every wait is bounded in wall time: on expiry the kernel records a status,
@@ -72,7 +73,13 @@ constexpr int kWarpMma0 = 9;         // MMA stream of Q tile 0; also owns TMEM a
 constexpr int kWarpMma1 = 10;        // MMA stream of Q tile 1
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsControl = 88;
-constexpr float kRescaleThreshold = 8.0f; // log2 units
+// Stale-max threshold (log2 units): the reference max moves (and O, l are
+// rescaled) only when a block's max exceeds it by more than this, so every
+// probability is at most 2^T. bf16 P reaches 2^127, so it takes T = 32: O and
+// l then stay finite in fp32 while N * 2^32 * max|V| < 2^128 (max|V| below
+// ~10^24 at N = 2^16). fp16 P ends below 2^16, so it keeps T = 8.
+template <bool kF16>
+constexpr float rescale_threshold() { return kF16 ? 8.0f : 32.0f; }
 // Each Q tile has its own 256-column TMEM allocation: S at column 0 (P overlays
 // its first 64 columns as packed bf16), O at column 128. MMAs issued by one
 // thread run in issue order; one thread issuing 128 x 128 x 16 MMAs back to
@@ -682,11 +689,11 @@ __device__ void softmax_role(uint32_t tm, int t, int wq, int lane, uint64_t* bar
             // or the shared half of P_t is rewritten.
             bool pb_pending = (i > first);
             // Move the reference max only when the block's max exceeds it by more
-            // than 2^8; then rescale O_t and l.
+            // than the threshold; then rescale O_t and l.
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 m_ref = m_tile;
-            } else if (m_tile > m_ref + kRescaleThreshold) {
+            } else if (m_tile > m_ref + rescale_threshold<kF16>()) {
                 alpha = ex2(m_ref - m_tile);
                 m_ref = m_tile;
             }

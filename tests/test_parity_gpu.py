@@ -102,6 +102,27 @@ def test_large_logits_stability(mult, causal, d):
     assert_parity(o, lse, o_ref, lse_ref, f"x{mult} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_every_block(causal, d):
+    """Scores fall by more than 50 log2 units per 128 keys, and the kernels visit
+    key blocks from the last to the first, so every block's max exceeds the
+    reference max by more than any stale-max threshold: O is rescaled in tensor
+    memory at every block, and the result is dominated by the first keys."""
+    B, H, N = 1, 2, 700
+    g = torch.Generator().manual_seed(31)
+    q = torch.zeros(B, H, N, d)
+    q[..., 0] = 3.0 + 2.0 * torch.rand(B, H, N, generator=g)
+    q[..., 1:] = 0.1 * torch.randn(B, H, N, d - 1, generator=g)
+    k = torch.randn(B, H, N, d, generator=g)
+    k[..., 0] = -0.75 * torch.arange(N, dtype=torch.float32)
+    v = torch.randn(B, H, N, d, generator=g)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    o, lse = run_guarded(q, k, v, 0.125, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, 0.125, causal)
+    assert_parity(o, lse, o_ref, lse_ref, f"rescale every block d={d} causal={causal}")
+
+
 def test_back_to_back_dependency():
     """A launch that reads the previous launch's output on the same stream sees all of it.
 
