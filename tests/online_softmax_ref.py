@@ -67,3 +67,39 @@ def blocked_online_attention(q, k, v, scale: float, causal: bool, block: int):
                     s[i + 1:] = -np.inf
                 o[b, h, i], lse[b, h, i], _ = blocked_online_row(s, v[b, h], block)
     return o, lse
+
+
+def stale_max_row(s: np.ndarray, v: np.ndarray, block: int, threshold_log2: float, reverse: bool):
+    """The same recurrence with a stale reference max: the reference m moves
+    only when a block's max exceeds it by more than `threshold_log2` (in log2
+    units, as the kernels count it), so each probability is at most
+    2^threshold; O and the LSE are the same quantities in exact arithmetic.
+    Blocks are visited last to first when `reverse` (the kernels' order).
+
+    Returns (o, lse, largest probability taken).
+    """
+    n = s.shape[0]
+    t = threshold_log2 * np.log(2.0)     # natural-log units
+    m = -np.inf
+    l = 0.0
+    acc = np.zeros(v.shape[1], dtype=np.float64)
+    p_max = 0.0
+    starts = list(range(0, n, block))
+    for j0 in (reversed(starts) if reverse else starts):
+        sb = s[j0:j0 + block]
+        vb = v[j0:j0 + block]
+        m_blk = float(np.max(sb))
+        if m == -np.inf:
+            if m_blk == -np.inf:        # every score so far masked
+                continue
+            m = m_blk
+        elif m_blk > m + t:             # move the reference: rescale the state
+            alpha = float(np.exp(m - m_blk))
+            l *= alpha
+            acc *= alpha
+            m = m_blk
+        p = np.exp(sb - m)
+        p_max = max(p_max, float(np.max(p)))
+        l += float(np.sum(p))
+        acc += p @ vb
+    return acc / l, m + np.log(l), p_max

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
-from online_softmax_ref import blocked_online_attention, blocked_online_row
+from online_softmax_ref import blocked_online_attention, blocked_online_row, stale_max_row
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -118,6 +118,36 @@ def test_blocked_online_equals_three_pass(causal, block):
     o, lse = blocked_online_attention(q, k, v, 0.25, causal, block)
     np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("threshold", [0.0, 8.0, 32.0])
+@pytest.mark.parametrize("reverse", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_stale_max_recurrence_equals_three_pass(threshold, reverse, causal):
+    """The kernels' stale-max rescaling (the reference max moves only when a
+    block's max exceeds it by more than a threshold, 32 or 8 log2 units in the
+    kernels) computes the same O and LSE as the three-pass definition, and no
+    probability it forms exceeds 2^threshold. Scores rise along the keys by
+    more than 32 log2 units per block, on top of logits of tens of units, so
+    the reference both stays stale and moves."""
+    B, H, N, d, block = 1, 2, 300, 16, 64
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((B, H, N, d)) * 4.0
+    k = rng.standard_normal((B, H, N, d)) * 4.0
+    k[..., 0] += 0.9 * np.arange(N)      # q_0 k_0 grows along the keys for rows with q_0 > 0
+    v = rng.standard_normal((B, H, N, d))
+    scale = 0.25
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    for h in range(H):
+        s_all = scale * (q[0, h] @ k[0, h].T)
+        for i in range(N):
+            s = s_all[i].copy()
+            if causal:
+                s[i + 1:] = -np.inf
+            o, lse, p_max = stale_max_row(s, v[0, h], block, threshold, reverse)
+            np.testing.assert_allclose(o, o_ref[0, h, i], rtol=1e-11, atol=1e-12)
+            assert lse == pytest.approx(lse_ref[0, h, i], rel=1e-12, abs=1e-12)
+            assert p_max <= 2.0 ** threshold * (1 + 1e-12)
 
 
 def test_matches_library_sdpa_fp64():
