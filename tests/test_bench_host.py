@@ -46,3 +46,33 @@ def test_clock_summary_flags_throttling():
 def test_job_throughput_is_whole_job_flops_per_second():
     # 2 ranks x 10 steps x 1e12 FLOP in 4 s: 5 TFLOP/s for the job
     assert abs(bench.job_throughput(1e12, steps=10, world=2, seconds=4.0) - 5.0) < 1e-12
+
+
+def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
+    """bench.py --impl reference (the fp64 oracle on the host cores) prints one
+    JSON line with the contract's keys, its own value repeated as the CPU
+    baseline and as an e2e figure with no host-device copies."""
+    import json
+
+    from blocked_online_softmax_gb300.workloads import BY_NAME
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+
+    class Args:
+        steps, warmup = 1, 1
+
+    w = BY_NAME["small_b1h2n256d64"]
+    assert bench.run_reference(Args(), w) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["config"] == bench.workload_config(w)
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
