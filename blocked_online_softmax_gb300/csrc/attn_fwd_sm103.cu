@@ -249,9 +249,7 @@ __device__ __forceinline__ Unit decode_unit(int k, const KernelArgs& a) {
 // Index >= total means no work is left. Where `unit` is set, the producer
 // also writes the decoded unit into the slot, so a reader can take it from
 // shared memory instead of repeating the integer divisions at a unit
-// change-over. The softmax warps do (2K causal +1.5 %); the MMA threads
-// decode for themselves (taking it there too measured 1 % slower at 8K
-// causal).
+// change-over; the softmax warps and the MMA threads both do.
 struct UnitRing {
     uint64_t* full;      // [kUnitRing] the producer has written the slot (1 arrival)
     uint64_t* empty;     // [kUnitRing] every reader has read it (kUnitReaders arrivals)
@@ -472,9 +470,9 @@ __device__ void mma_issuer(uint32_t tm, int t, const uint8_t* sQ, const uint8_t*
     for (int r = 0; ok; ++r) {
         int k;
         if (!ring.get(r, k, lim, abort_flag)) { ok = false; break; }
+        const Unit u = (k < total) ? ring.decoded(r) : Unit{};
         ring.release(r);
         if (k >= total) break;
-        const Unit u = decode_unit(k, a);
         const int first = (t == 0) ? u.first0 : 0;   // Q tile 0 skips the block past its diagonal
         if (!wait_or_abort(&bars[kBarQFull], r & 1, lim, abort_flag)) { ok = false; break; }
         int vprev = -1;                                // V stage of block i-1
